@@ -1,0 +1,433 @@
+"""Benchmark of the fused MoE finalize + rank sum + residual + RMSNorm on GB300.
+
+Headline (one JSON line on stdout): microseconds per call of the decode workload -- hidden 6144,
+256 experts, top-8, four tensor-parallel partials resident in this GPU's memory, each with its own
+GEMM2 rows, softmax top-k weights and shared-expert output; routed_scaling_factor 2.5, bf16 -- at
+128 tokens.  As in the benchmark of flashinfer PR #6631 (fi_finalize_bench.py), one step is one
+replay of a CUDA graph of 20 back-to-back launches (launched with PDL); each launch reads a
+different one of several input sets whose total size is over three times the L2, so every launch
+streams its inputs from HBM.  Also reported: the whole token sweep 1..128 (L2-warm, the page's own
+setting), the launch floor, the bandwidth workload (hidden 7168, 16384 tokens), the end-to-end time
+through the public API with host buffers, and the CPU oracle on the host cores.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+import torch.distributed as dist  # noqa: E402
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+GRAPH_LAUNCHES = 20
+METRIC = "fused finalize µs/call and achieved HBM GB/s (% of GB300 peak), H6144 top-8"
+UNIT = "µs/call"
+HEADLINE = dict(H=6144, K=8, R=4, E=256, rsf=2.5, shared=True, act_dtype=torch.bfloat16,
+                scale_dtype=torch.bfloat16, seed_base=100_000)
+HEADLINE_T = 128
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def algorithmic_bytes(case, quant="none") -> int:
+    """Bytes the definition must move per call: routing, valid GEMM2 rows, shared rows, residual,
+    gamma, residual_out and the normalised (or quantised) output."""
+    T, H = case.T, case.H
+    total = 0
+    for r in range(case.R):
+        sdt = 0 if case.scale[r] is None else case.scale[r].element_size()
+        total += T * case.K * (4 + sdt)
+        rows = case.gemm2[r].shape[0]
+        valid = int(((case.perm[r] >= 0) & (case.perm[r] < rows)).sum())
+        total += valid * H * 2
+        if case.shared[r] is not None:
+            total += T * H * 2
+    total += T * H * 2 + H * 2 + T * H * 2
+    total += {"none": T * H * 2, "fp8": T * H, "nvfp4": T * H // 2 + T * H // 16}[quant]
+    return total
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def capture_graph(fn, n=GRAPH_LAUNCHES):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(3):
+            fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fn(i)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, reps, warmup, launches=GRAPH_LAUNCHES):
+    """Median per-launch microseconds over `reps` replays (CUDA events on the replay stream)."""
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1000.0 / launches)
+    return statistics.median(times), times
+
+
+def make_sets(T, nsets, device, base=HEADLINE):
+    return [synth.make_case(f"decode-T{T}-set{i}", T=T, device=device, **{**base, "seed_base": base["seed_base"]
+                                                                           + 7919 * i}) for i in range(nsets)]
+
+
+def finalize_fn(mfr, case, outs, quant="none", qscale=None, sf_layout="row_major", kernel="auto"):
+    parts = [mfr.Partial(case.gemm2[r], case.perm[r], case.scale[r], case.shared[r]) for r in range(case.R)]
+
+    def call():
+        mfr.moe_finalize_fused(parts, case.residual, case.gamma, routed_scaling_factor=case.rsf, eps=case.eps,
+                               residual_out=outs[0], norm_out=outs[1], want_residual_out=outs[0] is not None,
+                               want_norm_out=outs[1] is not None, quant_mode=quant, quant_scale=qscale,
+                               sf_layout=sf_layout, quant_out=outs[2], sf_out=outs[3], pdl=True, kernel=kernel,
+                               check=False)
+    return call
+
+
+def alloc_outs(mfr, case, quant="none", sf_layout="row_major"):
+    dev = case.device
+    ro = torch.empty_like(case.residual)
+    no = torch.empty_like(case.residual) if quant == "none" else None
+    qo = sf = qs = None
+    if quant != "none":
+        qo = torch.empty(mfr.moe_finalize_quant_bytes(case.T, case.H, quant), dtype=torch.uint8, device=dev)
+        qs = torch.tensor([448.0 / 8 if quant == "fp8" else 448.0 * 6 / 8], device=dev)
+        if quant == "nvfp4":
+            sf = torch.empty(mfr.moe_finalize_sf_bytes(case.T, case.H, sf_layout), dtype=torch.uint8, device=dev)
+    return (ro, no, qo, sf), qs
+
+
+def traffic_for(kernel_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        from moe_finalize_residual_gb300 import build as b
+        import hashlib
+        h = hashlib.sha256()
+        for name in sorted(os.listdir(b.CSRC)):
+            h.update(open(os.path.join(b.CSRC, name), "rb").read())
+        e = d.get(kernel_name)
+        if e and e.get("source_sha256") == h.hexdigest():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+    return None
+
+
+def cpu_baseline(case, budget_s=12.0):
+    """The oracle, as it stands (single-threaded C), on the same workload; whole calls until the budget."""
+    import oracle
+    c = case.to("cpu")
+    oracle.finalize(c, 0, 1)  # build / load outside the timing
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.finalize(c)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 200:
+            break
+    return {"value": el / n * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole calls of the headline workload (T={c.T}, H={c.H}, R={c.R}, K={c.K}) "
+                      f"in {el:.1f} s on one host core"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle on the host cores, same workload, metric and unit.  Each step
+    times the oracle on a fixed sample of 16 of the call's 128 tokens and scales it to the whole call
+    (the oracle's cost is the same for every token), so the whole run stays within a few minutes."""
+    if rank != 0:
+        return
+    import oracle
+    case = synth.make_case(f"decode-T{HEADLINE_T}", T=HEADLINE_T, device="cpu", **HEADLINE)
+    oracle.finalize(case, 0, 1)
+    sample = 16
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        t0 = (i * sample) % HEADLINE_T
+        a = time.perf_counter()
+        oracle.finalize(case, t0, t0 + sample)
+        el = time.perf_counter() - a
+        if i >= args.warmup:
+            per_step.append(el / sample * HEADLINE_T * 1e6)
+    value = statistics.median(per_step)
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value / 1000.0, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+            "data": "synthetic",
+            "config": {"workload": f"decode H6144 E256 top-8 R4 shared rsf2.5 bf16, T={HEADLINE_T}",
+                       "global_batch": HEADLINE_T, "l2": "n/a (host)"},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(value, 1), "unit": UNIT,
+                             "sample": f"per step {sample} of the {HEADLINE_T} tokens of one call, scaled to the call"},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="headline only (no sweep, bandwidth, e2e, cpu)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import moe_finalize_residual_gb300 as mfr
+    peak, peak_kind = peaks()
+
+    # ---------------- headline: T=128 decode, rotating input sets > 3x L2 -----------------------
+    one = synth.make_case("probe", T=HEADLINE_T, device=dev, **HEADLINE)
+    bytes_call = algorithmic_bytes(one)
+    del one
+    nsets = max(2, -(-3 * L2_BYTES // bytes_call))
+    sets = make_sets(HEADLINE_T, nsets, dev)
+    outs = [alloc_outs(mfr, c)[0] for c in sets]
+    calls = [finalize_fn(mfr, c, o) for c, o in zip(sets, outs)]
+    plan = mfr.moe_finalize_plan([mfr.Partial(sets[0].gemm2[r], sets[0].perm[r], sets[0].scale[r], sets[0].shared[r])
+                                  for r in range(sets[0].R)], sets[0].residual, sets[0].gamma)
+    g = capture_graph(lambda i: calls[i % nsets]())
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for a, b in evs:
+            a.record()
+            g.replay()
+            b.record()
+        stop.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    per_launch = [a.elapsed_time(b) * 1000.0 / GRAPH_LAUNCHES for a, b in evs]
+    med_us = statistics.median(per_launch)
+    if world > 1:
+        t = torch.tensor([total_ms, med_us], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, med_us = float(t[0]), float(t[1])
+    achieved = bytes_call / (med_us * 1e-6) / 1e9
+    del g
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        # ---------------- token sweep, L2-warm (the pages' setting), and launch floors -------------
+        sweep = []
+        for T in (1, 4, 16, 32, 64, 128):
+            c = make_sets(T, 1, dev)[0]
+            o = alloc_outs(mfr, c)[0]
+            fn = finalize_fn(mfr, c, o)
+            gg = capture_graph(lambda i: fn())
+            us, _ = time_graph(gg, 50, 5)
+            p = mfr.moe_finalize_plan([mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r])
+                                       for r in range(c.R)], c.residual, c.gamma)
+            sweep.append({"T": T, "us": round(us, 3), "kernel": p["kernel"], "cluster": p["cluster"],
+                          "grid": p["grid"], "gbs_l2_warm": round(algorithmic_bytes(c) / (us * 1e-6) / 1e9, 1)})
+            del gg, c, o
+        gf = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=True))
+        floor_pdl, _ = time_graph(gf, 50, 5)
+        gf2 = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=False))
+        floor_nopdl, _ = time_graph(gf2, 50, 5)
+        del gf, gf2
+        for s in sweep:
+            s["x_floor"] = round(s["us"] / floor_pdl, 2)
+        extras["sweep_l2_warm"] = sweep
+        extras["launch_floor_us"] = {"pdl": round(floor_pdl, 3), "no_pdl": round(floor_nopdl, 3)}
+        del sets, outs, calls
+        torch.cuda.empty_cache()
+
+        # ---------------- bandwidth regime: H7168, T16384, R4, top-8 (inputs >> L2) ----------------
+        bw = []
+        c = synth.make_case("bandwidth-H7168-T16384", T=16384, H=7168, device=dev,
+                            **{k: v for k, v in synth.CONFIGS["bandwidth"].items() if k != "Ts"})
+        for quant, lay in (("none", "row_major"), ("fp8", "row_major"), ("nvfp4", "row_major"),
+                           ("nvfp4", "swizzled_128x4")):
+            o, qs = alloc_outs(mfr, c, quant, lay)
+            fn = finalize_fn(mfr, c, o, quant, qs, lay)
+            gg = capture_graph(lambda i: fn(), n=4)
+            us, _ = time_graph(gg, 10, 2, launches=4)
+            b = algorithmic_bytes(c, quant)
+            bw.append({"out": quant if quant != "nvfp4" else f"nvfp4-{lay}", "us": round(us, 1),
+                       "gb": round(b / 1e9, 3), "gbs": round(b / (us * 1e-6) / 1e9, 1),
+                       "frac": round(b / (us * 1e-6) / 1e9 / peak, 3)})
+            del gg, o
+        extras["bandwidth_H7168_T16384"] = bw
+        del c
+        torch.cuda.empty_cache()
+
+        # ---------------- end to end through the public API with host buffers ---------------------
+        c = make_sets(HEADLINE_T, 1, dev)[0]
+        host = {"gemm2": [x.cpu().pin_memory() for x in c.gemm2], "perm": [x.cpu().pin_memory() for x in c.perm],
+                "scale": [x.cpu().pin_memory() for x in c.scale], "shared": [x.cpu().pin_memory() for x in c.shared],
+                "residual": c.residual.cpu().pin_memory(), "gamma": c.gamma.cpu().pin_memory()}
+        h_ro = torch.empty_like(host["residual"]).pin_memory()
+        h_no = torch.empty_like(host["residual"]).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for k in ("gemm2", "perm", "scale", "shared") for x in host[k]) + \
+            host["residual"].numel() * 2 + host["gamma"].numel() * 2
+        d2h = 2 * h_ro.numel() * 2
+
+        def e2e_step():
+            for r in range(c.R):
+                c.gemm2[r].copy_(host["gemm2"][r], non_blocking=True)
+                c.perm[r].copy_(host["perm"][r], non_blocking=True)
+                c.scale[r].copy_(host["scale"][r], non_blocking=True)
+                c.shared[r].copy_(host["shared"][r], non_blocking=True)
+            c.residual.copy_(host["residual"], non_blocking=True)
+            c.gamma.copy_(host["gamma"], non_blocking=True)
+            ro, no, _, _ = mfr.moe_finalize_fused(
+                [mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r]) for r in range(c.R)],
+                c.residual, c.gamma, routed_scaling_factor=c.rsf, eps=c.eps)
+            h_ro.copy_(ro, non_blocking=True)
+            h_no.copy_(no, non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = 50
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e2e_us = a.elapsed_time(b) * 1000.0 / n_e2e
+        extras["e2e"] = {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                         "d2h_bytes_per_step": int(d2h)}
+        extras["cpu_baseline"] = cpu_baseline(c)
+        del c
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(med_us, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": f"decode H6144 E256 top-8 R4 shared rsf2.5 bf16, T={HEADLINE_T}",
+                       "global_batch": HEADLINE_T * world, "per_gpu_tokens": HEADLINE_T, "hidden": 6144,
+                       "top_k": 8, "partials": 4, "step": f"one CUDA-graph replay of {GRAPH_LAUNCHES} launches (PDL)",
+                       "l2": f"inputs larger than L2: {nsets} rotating input sets, {nsets * bytes_call / 1e6:.0f} MB",
+                       "kernel": plan["kernel"], "cluster": plan["cluster"], "grid": plan["grid"],
+                       "parallelism": f"dp{world} (token shards, no collective)"},
+            "mean_us": round(total_ms * 1000.0 / (args.steps * GRAPH_LAUNCHES), 3),
+            "tokens_per_s": round(HEADLINE_T * world / (med_us * 1e-6)),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic_for(f"{plan['kernel']}_decode_T128"),
+                         "peak_kind": f"of {peak_kind}", "algorithmic_bytes_per_launch": bytes_call},
+            "gpu_launches": args.steps * GRAPH_LAUNCHES,
+            "clocks": clk.summary(),
+            "timed_wall_s": round(wall, 3),
+        }
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,394 @@
+// C ABI of the fused MoE finalize: argument validation (nothing is enqueued on error), launch
+// planning for the two kernels, dispatch, size queries and status strings.
+//
+// Validation follows the guards named on the pages: the hidden size must be a multiple of the
+// 128-bit vector width, since no tail is read or written partially (flashinfer PR #3385, review of
+// the one-shot dispatch: reject token_dim not divisible by 16 / sizeof(T)); only the LINEAR and
+// SWIZZLED_128x4 scale layouts are accepted (same review, layout whitelist); optional outputs may
+// be NULL (same review: guard the prenormed output); 4 < topK <= 64 bounds the small-batch kernel
+// of flashinfer PR #6546 (here any 1 <= K <= 64 is accepted).
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <map>
+#include <tuple>
+
+#include "mfr_launch.h"
+#include "moe_finalize.h"
+
+namespace mfr {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::tuple<int, int, int, int, int>, int> g_cluster_ok;  // (dev, act, C, block, smem) -> clusters
+std::map<std::tuple<int, int, int, int>, int> g_stream_bps;       // (dev, act, block, smem) -> blocks/SM
+
+int device_info(DeviceInfo* out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_devices.find(dev);
+  if (it == g_devices.end()) {
+    DeviceInfo d;
+    int major = 0;
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return fail(MFR_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    if (major < 10) return fail(MFR_ERR_UNSUPPORTED, "device %d has compute capability %d.x; built for sm_103a", dev, major);
+    it = g_devices.emplace(dev, d).first;
+  }
+  *out = it->second;
+  *dev_out = dev;
+  return MFR_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int validate(const mfr_args* a) {
+  if (a == nullptr) return fail(MFR_ERR_INVALID_ARG, "args is NULL");
+  if (a->T < 0) return fail(MFR_ERR_INVALID_ARG, "T = %d < 0", a->T);
+  if (a->H < 8 || a->H > MFR_MAX_HIDDEN || a->H % 8 != 0)
+    return fail(MFR_ERR_INVALID_ARG, "H = %d must be a multiple of 8 in [8, %d]", a->H, MFR_MAX_HIDDEN);
+  if (a->K < 1 || a->K > MFR_MAX_TOP_K) return fail(MFR_ERR_INVALID_ARG, "K = %d outside [1, %d]", a->K, MFR_MAX_TOP_K);
+  if (a->R < 1 || a->R > MFR_MAX_PARTIALS)
+    return fail(MFR_ERR_INVALID_ARG, "R = %d outside [1, %d]", a->R, MFR_MAX_PARTIALS);
+  if (a->act_dtype != MFR_BF16 && a->act_dtype != MFR_FP16)
+    return fail(MFR_ERR_UNSUPPORTED, "act_dtype %d: only MFR_BF16 and MFR_FP16", a->act_dtype);
+  if (a->scale_dtype != MFR_FP32 && a->scale_dtype != MFR_BF16 && a->scale_dtype != MFR_FP16)
+    return fail(MFR_ERR_UNSUPPORTED, "scale_dtype %d unknown", a->scale_dtype);
+  if (a->quant_mode < MFR_QUANT_NONE || a->quant_mode > MFR_QUANT_NVFP4)
+    return fail(MFR_ERR_UNSUPPORTED, "quant_mode %d unknown", a->quant_mode);
+  if (a->quant_mode == MFR_QUANT_NVFP4) {
+    if (a->sf_layout != MFR_SF_ROW_MAJOR && a->sf_layout != MFR_SF_SWIZZLED_128x4)
+      return fail(MFR_ERR_UNSUPPORTED, "sf_layout %d: only ROW_MAJOR and SWIZZLED_128x4", a->sf_layout);
+    if (a->H % 16 != 0) return fail(MFR_ERR_INVALID_ARG, "NVFP4 needs H %% 16 == 0 (H = %d)", a->H);
+  }
+  if (a->flags & ~static_cast<uint32_t>(MFR_FLAG_PDL | MFR_FLAG_ROUTING_READY))
+    return fail(MFR_ERR_INVALID_ARG, "unknown flag bits 0x%x", a->flags);
+  if (a->kernel < MFR_KERNEL_AUTO || a->kernel > MFR_KERNEL_STREAM)
+    return fail(MFR_ERR_INVALID_ARG, "kernel %d unknown", a->kernel);
+  if (a->T == 0) return MFR_OK;  // nothing to read or write
+  if (a->partials == nullptr) return fail(MFR_ERR_INVALID_ARG, "partials is NULL");
+  const uintptr_t sdt_align = a->scale_dtype == MFR_FP32 ? 4 : 2;
+  for (int r = 0; r < a->R; ++r) {
+    const mfr_partial& P = a->partials[r];
+    if (P.perm_idx == nullptr) return fail(MFR_ERR_INVALID_ARG, "partials[%d].perm_idx is NULL", r);
+    if (P.num_rows < 0) return fail(MFR_ERR_INVALID_ARG, "partials[%d].num_rows < 0", r);
+    if (P.num_rows > 0 && P.gemm2_out == nullptr)
+      return fail(MFR_ERR_INVALID_ARG, "partials[%d].gemm2_out is NULL", r);
+    if (P.num_rows > (int64_t{1} << 40) / a->H) return fail(MFR_ERR_INVALID_ARG, "partials[%d].num_rows too large", r);
+    if (!aligned(P.gemm2_out, 16)) return fail(MFR_ERR_INVALID_ARG, "partials[%d].gemm2_out not 16-byte aligned", r);
+    if (!aligned(P.perm_idx, 4)) return fail(MFR_ERR_INVALID_ARG, "partials[%d].perm_idx not 4-byte aligned", r);
+    if (!aligned(P.expert_scale, sdt_align))
+      return fail(MFR_ERR_INVALID_ARG, "partials[%d].expert_scale misaligned", r);
+    if (!aligned(P.shared_out, 16)) return fail(MFR_ERR_INVALID_ARG, "partials[%d].shared_out not 16-byte aligned", r);
+  }
+  if (a->residual == nullptr || a->gamma == nullptr) return fail(MFR_ERR_INVALID_ARG, "residual and gamma are required");
+  if (!aligned(a->residual, 16) || !aligned(a->gamma, 16) || !aligned(a->residual_out, 16) || !aligned(a->norm_out, 16))
+    return fail(MFR_ERR_INVALID_ARG, "residual, gamma, residual_out and norm_out must be 16-byte aligned");
+  if (a->quant_mode != MFR_QUANT_NONE) {
+    if (a->quant_out == nullptr || a->quant_scale == nullptr)
+      return fail(MFR_ERR_INVALID_ARG, "quantisation needs quant_out and quant_scale");
+    if (a->quant_mode == MFR_QUANT_NVFP4 && a->sf_out == nullptr)
+      return fail(MFR_ERR_INVALID_ARG, "NVFP4 needs sf_out (moe_finalize_sf_bytes bytes)");
+    if (!aligned(a->quant_scale, 4) || !aligned(a->quant_out, a->quant_mode == MFR_QUANT_FP8_E4M3 ? 4 : 2))
+      return fail(MFR_ERR_INVALID_ARG, "quant_scale or quant_out misaligned");
+  }
+  if (a->residual_out == nullptr && a->norm_out == nullptr && a->quant_mode == MFR_QUANT_NONE)
+    return fail(MFR_ERR_INVALID_ARG, "no output requested");
+  return MFR_OK;
+}
+
+void fill_params(const mfr_args* a, KParams* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->T = a->T;
+  p->H = a->H;
+  p->K = a->K;
+  p->R = a->R;
+  uint32_t mask = 0;
+  for (int r = 0; r < a->R; ++r) {
+    const mfr_partial& P = a->partials[r];
+    p->part[r].gemm2 = static_cast<const uint8_t*>(P.gemm2_out);
+    p->part[r].rows = P.gemm2_out ? P.num_rows : 0;
+    p->part[r].perm = P.perm_idx;
+    p->part[r].scale = P.expert_scale;
+    p->part[r].shared = static_cast<const uint8_t*>(P.shared_out);
+    if (P.shared_out) mask |= 1u << r;
+  }
+  p->shared_mask = mask;
+  p->nslots = a->R * a->K + __builtin_popcount(mask);
+  p->residual = static_cast<const uint8_t*>(a->residual);
+  p->gamma = static_cast<const uint8_t*>(a->gamma);
+  p->residual_out = static_cast<uint8_t*>(a->residual_out);
+  p->norm_out = static_cast<uint8_t*>(a->norm_out);
+  p->quant_out = static_cast<uint8_t*>(a->quant_out);
+  p->sf_out = static_cast<uint8_t*>(a->sf_out);
+  p->quant_scale = a->quant_scale;
+  p->scale_dtype = a->scale_dtype;
+  p->quant = a->quant_mode;
+  p->sf_layout = a->sf_layout;
+  p->pdl = (a->flags & MFR_FLAG_PDL) ? 1 : 0;
+  p->routing_early = (p->pdl && (a->flags & MFR_FLAG_ROUTING_READY)) ? 1 : 0;
+  p->rsf = a->routed_scaling_factor;
+  p->eps = a->eps;
+}
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+int pow2_ceil(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Token count up to which the cluster kernel is chosen automatically.
+constexpr int kClusterMaxTokens = 256;
+constexpr int kMaxCluster = 16;
+
+// Cluster kernel: C CTAs per token, each holding every row of its hidden slice in shared memory.
+bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
+  const int nvec = a->H / 8;
+  const int unit = (a->H % 16 == 0) ? 2 : 1;  // slices start on 16-element blocks when H allows
+  const int ns = p->nslots;
+  const int c0 = std::min(kMaxCluster, pow2_ceil(ceil_div(2 * d.sms, std::max(1, a->T))));
+  for (int C = c0; C <= kMaxCluster; C *= 2) {
+    const int slice_vec = align_up(ceil_div(nvec, C), unit);
+    if ((C - 1) * slice_vec >= nvec && C > 1) continue;  // a CTA would get no hidden elements
+    const int block = std::max(64, align_up(ceil_div(slice_vec * 8, 4), 32));
+    const int off_src = align_up(ns * slice_vec * 16, 16);
+    const int off_scale = off_src + ns * 8;
+    const int off_flag = off_scale + ns * 4;
+    const int off_red = align_up(off_flag + ns, 16);
+    const int smem = align_up(off_red + 34 * 4, 128);
+    if (block > 1024 || smem > d.smem_optin) continue;
+    LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
+    if (C > 1) {
+      const auto key = std::make_tuple(dev, a->act_dtype, C, block, smem);
+      int n;
+      {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_cluster_ok.find(key);
+        n = (it == g_cluster_ok.end()) ? -1 : it->second;
+      }
+      if (n < 0) {
+        n = cluster_kernel_max_active_clusters(a->act_dtype, geo);
+        std::lock_guard<std::mutex> lock(g_mu);
+        g_cluster_ok[key] = n;
+      }
+      if (n < 1) continue;
+    }
+    p->slice_vec = slice_vec;
+    p->off_src = off_src;
+    p->off_scale = off_scale;
+    p->off_flag = off_flag;
+    p->off_red = off_red;
+    *g = geo;
+    return true;
+  }
+  return false;
+}
+
+// Stream kernel: persistent CTAs, hidden streamed in chunks through a stage ring.
+bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
+  const int ncw = 4;
+  const int block = 32 * (2 + ncw);
+  const int ns = p->nslots;
+  const int D = 4;
+  const int ring_bytes = align_up(((ns * 13 + 3) & ~3) + 4, 16);
+  for (int CH = 128 * ncw; CH >= 64; CH /= 2) {
+    const int ch = std::min(CH, align_up(a->H, 16));
+    const int stage_bytes = (ns + 1) * ch * 2;
+    for (int NS = 4; NS >= 2; --NS) {
+      const int bar_bytes = 8 * (2 * NS + 2 * D + 3) + 8;
+      const int off_stage = align_up(bar_bytes, 128);
+      const int off_ring = off_stage + NS * stage_bytes;
+      const int off_gamma = align_up(off_ring + D * ring_bytes, 16);
+      const int off_stash = off_gamma + align_up(a->H * 2, 16);
+      const int off_sred = off_stash + align_up(a->H * 2, 16);
+      const int smem = align_up(off_sred + 2 * 32 * 4, 128);
+      if (smem > d.smem_optin) continue;
+      LaunchGeom geo{0, block, 1, smem, d.smem_optin};
+      const auto key = std::make_tuple(dev, a->act_dtype, block, smem);
+      int bps;
+      {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_stream_bps.find(key);
+        bps = (it == g_stream_bps.end()) ? -1 : it->second;
+      }
+      if (bps < 0) {
+        bps = stream_kernel_blocks_per_sm(a->act_dtype, geo);
+        std::lock_guard<std::mutex> lock(g_mu);
+        g_stream_bps[key] = bps;
+      }
+      if (bps < 1) continue;
+      geo.grid = std::min(a->T, d.sms * bps);
+      p->chunk = ch;
+      p->stages = NS;
+      p->rdepth = D;
+      p->stage_bytes = stage_bytes;
+      p->ring_bytes = ring_bytes;
+      p->off_bar = 0;
+      p->off_stage = off_stage;
+      p->off_ring = off_ring;
+      p->off_gamma = off_gamma;
+      p->off_stash = off_stash;
+      p->off_sred = off_sred;
+      *g = geo;
+      return true;
+    }
+  }
+  return false;
+}
+
+int make_plan(const mfr_args* a, KParams* p, LaunchGeom* g, int* kernel) {
+  int st = validate(a);
+  if (st != MFR_OK) return st;
+  if (a->T == 0) {
+    *kernel = MFR_KERNEL_AUTO;
+    return MFR_OK;
+  }
+  DeviceInfo d;
+  int dev = 0;
+  if ((st = device_info(&d, &dev)) != MFR_OK) return st;
+  fill_params(a, p);
+  const bool want_cluster =
+      a->kernel == MFR_KERNEL_CLUSTER || (a->kernel == MFR_KERNEL_AUTO && a->T <= kClusterMaxTokens);
+  if (want_cluster && plan_cluster(a, d, dev, p, g)) {
+    *kernel = MFR_KERNEL_CLUSTER;
+    return MFR_OK;
+  }
+  if (a->kernel != MFR_KERNEL_CLUSTER && plan_stream(a, d, dev, p, g)) {
+    *kernel = MFR_KERNEL_STREAM;
+    return MFR_OK;
+  }
+  if (a->kernel == MFR_KERNEL_AUTO && plan_cluster(a, d, dev, p, g)) {
+    *kernel = MFR_KERNEL_CLUSTER;
+    return MFR_OK;
+  }
+  return fail(MFR_ERR_UNSUPPORTED, "no kernel fits T=%d H=%d K=%d R=%d in shared memory (kernel %d)", a->T, a->H,
+              a->K, a->R, a->kernel);
+}
+
+__global__ void empty_kernel(int pdl) {
+  if (pdl) {
+    pdl_launch_dependents();
+    pdl_wait();
+  }
+}
+
+}  // namespace
+}  // namespace mfr
+
+using namespace mfr;
+
+extern "C" {
+
+int moe_finalize_fused(const mfr_args* args, struct CUstream_st* stream) {
+  KParams p;
+  LaunchGeom g{};
+  int kernel = 0;
+  int st = make_plan(args, &p, &g, &kernel);
+  if (st != MFR_OK || args->T == 0) return st;
+  cudaError_t e = (kernel == MFR_KERNEL_CLUSTER) ? launch_cluster_kernel(args->act_dtype, p, g, stream)
+                                                 : launch_stream_kernel(args->act_dtype, p, g, stream);
+  if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return MFR_OK;
+}
+
+int moe_finalize_plan(const mfr_args* args, mfr_plan* plan) {
+  if (plan == nullptr) return fail(MFR_ERR_INVALID_ARG, "plan is NULL");
+  KParams p;
+  LaunchGeom g{};
+  int kernel = 0;
+  int st = make_plan(args, &p, &g, &kernel);
+  if (st != MFR_OK) return st;
+  plan->kernel = kernel;
+  plan->grid = g.grid;
+  plan->cluster = g.cluster;
+  plan->block = g.block;
+  plan->smem_bytes = g.smem;
+  plan->chunk = kernel == MFR_KERNEL_STREAM ? p.chunk : p.slice_vec * 8;
+  plan->stages = kernel == MFR_KERNEL_STREAM ? p.stages : 1;
+  return MFR_OK;
+}
+
+int64_t moe_finalize_sf_bytes(int32_t T, int32_t H, int32_t sf_layout) {
+  if (T < 0 || H <= 0 || H % 16 != 0) return fail(MFR_ERR_INVALID_ARG, "T >= 0 and H a positive multiple of 16");
+  const int64_t cols = H / 16;
+  if (sf_layout == MFR_SF_ROW_MAJOR) return static_cast<int64_t>(T) * cols;
+  if (sf_layout == MFR_SF_SWIZZLED_128x4) return ((static_cast<int64_t>(T) + 127) / 128) * 128 * ((cols + 3) / 4) * 4;
+  return fail(MFR_ERR_UNSUPPORTED, "sf_layout %d unknown", sf_layout);
+}
+
+int64_t moe_finalize_quant_bytes(int32_t T, int32_t H, int32_t quant_mode) {
+  if (T < 0 || H <= 0) return fail(MFR_ERR_INVALID_ARG, "T >= 0 and H > 0");
+  switch (quant_mode) {
+    case MFR_QUANT_NONE: return 0;
+    case MFR_QUANT_FP8_E4M3: return static_cast<int64_t>(T) * H;
+    case MFR_QUANT_NVFP4:
+      if (H % 16 != 0) return fail(MFR_ERR_INVALID_ARG, "NVFP4 needs H %% 16 == 0");
+      return static_cast<int64_t>(T) * H / 2;
+    default: return fail(MFR_ERR_UNSUPPORTED, "quant_mode %d unknown", quant_mode);
+  }
+}
+
+const char* moe_finalize_status_string(int status) {
+  switch (status) {
+    case MFR_OK: return "MFR_OK";
+    case MFR_ERR_INVALID_ARG: return "MFR_ERR_INVALID_ARG: invalid argument";
+    case MFR_ERR_UNSUPPORTED: return "MFR_ERR_UNSUPPORTED: unsupported combination";
+    case MFR_ERR_CUDA: return "MFR_ERR_CUDA: CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_finalize_last_error(void) { return g_last_error; }
+
+int moe_finalize_empty_launch(struct CUstream_st* stream, uint32_t flags) {
+  const int pdl = (flags & MFR_FLAG_PDL) ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, empty_kernel, pdl);
+  if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "empty launch: %s", cudaGetErrorString(e));
+  return MFR_OK;
+}
+
+int moe_finalize_read_timeouts(uint32_t* count) {
+  if (count == nullptr) return fail(MFR_ERR_INVALID_ARG, "count is NULL");
+  unsigned int c = 0;
+  cudaError_t e = read_and_reset_timeouts(&c);
+  if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "reading the timeout counter: %s", cudaGetErrorString(e));
+  *count = c;
+  return MFR_OK;
+}
+
+int moe_finalize_abi_version(void) { return MFR_ABI_VERSION; }
+
+}  // extern "C"

@@ -121,6 +121,7 @@ def _declare(L):
     L.oracle_e4m3_to_f32.restype = ctypes.c_float
     L.oracle_e2m1_to_f32.argtypes = [ctypes.c_uint8]
     L.oracle_e2m1_to_f32.restype = ctypes.c_float
+    L.oracle_sf_offsets.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P]
     L.oracle_fmaf.argtypes = [ctypes.c_float] * 3
     L.oracle_fmaf.restype = ctypes.c_float
 
@@ -184,6 +185,13 @@ def sf_bytes(T: int, H: int, layout: int) -> int:
 
 def sf_offset(m: int, k: int, H: int, layout: int) -> int:
     return int(lib().oracle_sf_offset(m, k, H, layout))
+
+
+def sf_offsets(T: int, H: int, layout: int) -> np.ndarray:
+    """[T, H/16] array of block-scale byte offsets."""
+    out = np.zeros((T, H // 16), dtype=np.int64)
+    lib().oracle_sf_offsets(T, H, layout, out.ctypes.data)
+    return out
 
 
 def quantize(norm_bits: np.ndarray, act_dtype, quant: int, qscale: float, sf_layout: int = SF_ROW_MAJOR,

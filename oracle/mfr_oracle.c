@@ -362,3 +362,9 @@ void oracle_f32_to_e2m1_array(const float* x, uint8_t* y, int64_t n) {
   for (int64_t i = 0; i < n; ++i) y[i] = oracle_f32_to_e2m1(x[i]);
 }
 float oracle_fmaf(float a, float b, float c) { return fmaf(a, b, c); }
+
+/* Offsets of every (row, block) scale of a T x H tensor, row-major order of (m, k). */
+void oracle_sf_offsets(int64_t T, int64_t H, int layout, int64_t* out) {
+  for (int64_t m = 0; m < T; ++m)
+    for (int64_t k = 0; k < H / 16; ++k) out[m * (H / 16) + k] = oracle_sf_offset(m, k, H, layout);
+}

@@ -1,0 +1,388 @@
+"""Parity of the CUDA library (through its C ABI) with the CPU oracle, on every workload family.
+
+residual_out must be bit-identical to the oracle; norm_out within 1 ulp of the activation type
+(only the order of the RMS sum of squares differs); the mean absolute error of norm_out against an
+FP64 evaluation no worse than the oracle's own (1% slack); quantised bytes bit-identical to the
+oracle's quantiser applied to the kernel's own norm_out.  Every output sits between canary guards.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import (CANARY, Guarded, as_f64, bits16, check_against_oracle, check_quant, partials_of,
+                     quant_scale_for, run, subcase, ulp_distance)
+
+pytestmark = pytest.mark.gpu
+KERNELS = ["cluster", "stream"]
+
+
+def on_gpu(case):
+    return case.to("cuda")
+
+
+def check_case(case, kernel, **kw):
+    res = run(on_gpu(case), kernel=kernel, **kw)
+    assert res.guards_ok, "an output guard was overwritten"
+    return res, check_against_oracle(case, res)
+
+
+# --------------------------------------------------------------------------------------------
+# Workload families
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("pdl", [True, False])
+@pytest.mark.parametrize("kernel", KERNELS + ["auto"])
+def test_tiny(kernel, pdl):
+    check_case(next(synth.config_cases("tiny")), kernel, pdl=pdl)
+
+
+@pytest.mark.parametrize("T", synth.CONFIGS["decode"]["Ts"])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_decode(T, kernel):
+    check_case(next(synth.config_cases("decode", Ts=(T,))), kernel)
+
+
+def _masked_cases():
+    out = []
+    for case_T in (1, 16):
+        for K in (6, 8, 10):
+            for act in (torch.float16, torch.bfloat16):
+                for R in (2, 4):
+                    for sdt in (torch.float32, torch.bfloat16):
+                        out.append((case_T, K, act, R, sdt))
+    for i, T in enumerate((64, 128)):
+        for K in (6, 8, 10):
+            out.append((T, K, (torch.float16, torch.bfloat16)[(K + i) % 2], (2, 4)[(K // 2 + i) % 2],
+                        (torch.float32, torch.bfloat16)[i]))
+    return out
+
+
+@pytest.mark.parametrize("T,K,act,R,sdt", _masked_cases())
+def test_masked(T, K, act, R, sdt):
+    c = dict(synth.CONFIGS["masked"])
+    c.pop("Ts")
+    case = synth.make_case(f"masked-T{T}", T=T, K=K, R=R, act_dtype=act, scale_dtype=sdt, **c)
+    for kernel in KERNELS:
+        res, _ = check_case(case, kernel)
+        assert not np.isnan(as_f64(res.residual_out, act)).any(), "a NaN row behind a masked route leaked"
+
+
+@pytest.mark.parametrize("T", synth.CONFIGS["highk"]["Ts"])
+@pytest.mark.parametrize("shape", synth.HIGHK_SHAPES)
+def test_highk(shape, T):
+    H, E, K = shape
+    c = dict(synth.CONFIGS["highk"])
+    c.pop("Ts")
+    case = synth.make_case(f"highk-T{T}", T=T, H=H, E=E, K=K, **c)
+    for kernel in KERNELS:
+        check_case(case, kernel)
+
+
+# --------------------------------------------------------------------------------------------
+# Quantised outputs
+# --------------------------------------------------------------------------------------------
+
+QUANTS = [("fp8", "row_major"), ("nvfp4", "row_major"), ("nvfp4", "swizzled_128x4")]
+
+
+@pytest.mark.parametrize("quant,layout", QUANTS)
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("act", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("T", [1, 37, 130])
+def test_quant_small(T, act, kernel, quant, layout):
+    case = synth.make_case("q", T=T, H=1024, K=8, R=2, E=64, act_dtype=act, rsf=2.5, shared=True)
+    want = oracle.finalize(case)
+    qs = quant_scale_for(want["norm_out"], act, quant)
+    res = run(on_gpu(case), kernel=kernel, quant=quant, qscale=qs, sf_layout=layout)
+    assert res.guards_ok
+    check_against_oracle(case, res, want)
+    check_quant(res, act, quant, qs, layout, T, case.H, want_norm=want["norm_out"])
+
+
+@pytest.mark.parametrize("quant,layout", QUANTS)
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_quant_without_norm_out(kernel, quant, layout):
+    """norm_out may be omitted when a quantised output is requested; the quantised bytes are then those
+    of the oracle's norm_out wherever the kernel's would agree (checked here by a second run)."""
+    case = synth.make_case("qn", T=20, H=2048, K=6, R=1, E=32, rsf=1.0)
+    g = on_gpu(case)
+    qs = 37.5
+    full = run(g, kernel=kernel, quant=quant, qscale=qs, sf_layout=layout)
+    only = run(g, kernel=kernel, quant=quant, qscale=qs, sf_layout=layout, norm_out=False, residual_out=False)
+    assert only.guards_ok and full.guards_ok
+    assert np.array_equal(full.quant_out, only.quant_out)
+    if quant == "nvfp4":
+        assert np.array_equal(full.sf_out, only.sf_out)
+
+
+def _gamma_sweep_case(gamma_bits: np.ndarray, T=2):
+    """Rows of +-1 with every route masked and eps = 0, so rstd = 1 exactly and norm_out == +-gamma:
+    the quantiser then sees every chosen bf16 value."""
+    H = gamma_bits.size
+    case = synth.make_case("sweep", T=T, H=H, K=1, R=1, E=4, rsf=1.0)
+    case.perm = [torch.full((T, 1), -1, dtype=torch.int32)]
+    sign = torch.ones(T, H)
+    sign[1::2] = -1
+    case.residual = sign.to(torch.bfloat16)
+    case.gamma = torch.from_numpy(gamma_bits.astype(np.uint16).view(np.int16)).view(torch.bfloat16)
+    case.eps = 0.0
+    return case
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.75, 448.0 / 3.0, 2.0 ** -7])
+@pytest.mark.parametrize("quant", ["fp8", "nvfp4"])
+def test_codec_sweep_all_bf16(quant, scale):
+    """Every finite bf16 value passes through the kernel's FP8 / NVFP4 conversion and must encode as the
+    oracle's software codec says (ties to even, saturation, signed zero, subnormals)."""
+    allbits = np.arange(65536, dtype=np.uint32)
+    finite = ((allbits & 0x7F80) != 0x7F80)
+    vals = allbits[finite]
+    vals = np.concatenate([vals, np.zeros((-vals.size) % 32768, dtype=np.uint32)])
+    for chunk in vals.reshape(-1, 32768):
+        case = _gamma_sweep_case(chunk)
+        res = run(on_gpu(case), kernel="cluster", quant=quant, qscale=scale)
+        want_norm = np.stack([chunk.astype(np.uint16), (chunk ^ 0x8000).astype(np.uint16)])
+        assert np.array_equal(res.norm_out, want_norm)
+        check_quant(res, torch.bfloat16, quant, scale, "row_major", 2, case.H)
+
+
+# --------------------------------------------------------------------------------------------
+# Full sizes: sampled tokens against the oracle
+# --------------------------------------------------------------------------------------------
+
+def _sample_tokens(T, n=40, seed=0):
+    g = np.random.default_rng(seed)
+    picks = {0, 1, T - 1, T // 2, 127 % T, 128 % T}
+    picks.update(int(x) for x in g.choice(T, size=min(T, n), replace=False))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("H", [6144, 7168])
+@pytest.mark.parametrize("T", [1024, 4096, 16384])
+def test_bandwidth_sampled(T, H):
+    c = dict(synth.CONFIGS["bandwidth"])
+    c.pop("Ts")
+    case = synth.make_case(f"bandwidth-H{H}-T{T}", T=T, H=H, device="cuda", **c)
+    toks = _sample_tokens(T)
+    sub = subcase(case, toks)
+    want = oracle.finalize(sub)
+    for kernel in ("auto", "stream"):
+        res = run(case, kernel=kernel)
+        assert res.guards_ok
+        check_against_oracle(sub, res, want, tokens=toks)
+    # quantised variants at the same size (scale: amax of norm_out taken as 8, see the design notes)
+    for quant, layout, qs in (("fp8", "row_major", 448.0 / 8), ("nvfp4", "row_major", 448.0 * 6 / 8),
+                              ("nvfp4", "swizzled_128x4", 448.0 * 6 / 8)):
+        res = run(case, kernel="auto", quant=quant, qscale=qs, sf_layout=layout)
+        assert res.guards_ok
+        check_against_oracle(sub, res, want, tokens=toks)
+        lay = oracle.SF_ROW_MAJOR if layout == "row_major" else oracle.SF_SWIZZLED_128x4
+        qm = oracle.QUANT_FP8 if quant == "fp8" else oracle.QUANT_NVFP4
+        q_own, sf_own = oracle.quantize(res.norm_out[toks], case.act_dtype, qm, qs, oracle.SF_ROW_MAJOR)
+        if quant == "fp8":
+            assert np.array_equal(res.quant_out.reshape(T, H)[toks], q_own)
+        else:
+            assert np.array_equal(res.quant_out.reshape(T, H // 2)[toks], q_own)
+            offs = oracle.sf_offsets(T, H, lay)[toks]
+            assert np.array_equal(res.sf_out[offs.reshape(-1)], sf_own)
+        del res
+    torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------------------------
+# Edge cases
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_empty_batch_writes_nothing(kernel):
+    case = synth.make_case("e", T=3, H=256, K=2, R=1, E=8)
+    g = on_gpu(case)
+    import moe_finalize_residual_gb300 as mfr
+    out = Guarded(3 * 256 * 2, "cuda", torch.bfloat16, (3, 256))
+    empty = g.residual[:0]
+    parts = [mfr.Partial(g.gemm2[0], g.perm[0][:0], g.scale[0][:0], None)]
+    mfr.moe_finalize_fused(parts, empty, g.gamma, residual_out=out.view[:0], norm_out=out.view[:0], kernel=kernel)
+    torch.cuda.synchronize()
+    assert out.guards_intact() and np.all(out.payload() == CANARY)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("H", [8, 24, 776, 4104, 32768])
+def test_ragged_and_extreme_hidden(H, kernel):
+    """H not a multiple of any slice or chunk size, the smallest H and the largest."""
+    T = 3 if H < 32768 else 2
+    case = synth.make_case("rag", T=T, H=H, K=4, R=2, E=16, rsf=2.5, shared=True)
+    check_case(case, kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_max_slots(kernel):
+    """R = 8 partials of K = 64 routes each, every one with a shared row: 520 rows per token."""
+    case = synth.make_case("max", T=5, H=2048, K=64, R=8, E=128, rsf=0.5, shared=True, scale_dtype=torch.float16)
+    check_case(case, kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_single_route_identity(kernel):
+    case = synth.make_case("id", T=9, H=512, K=1, R=1, E=8, scale_dtype=None, rsf=1.0)
+    res, _ = check_case(case, kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_out_of_range_and_negative_indices(kernel):
+    case = synth.make_case("oor", T=6, H=1024, K=8, R=3, E=32, rsf=2.5, shared=True)
+    for r in range(case.R):
+        p = case.perm[r].clone()
+        rows = case.gemm2[r].shape[0]
+        p[0, 0] = rows          # one past the end
+        p[1, 3] = rows + 12345
+        p[2, 7] = -1
+        p[3, 1] = -7
+        p[4, :] = -1            # a token with no valid route in this partial
+        case.perm[r] = p
+    res, _ = check_case(case, kernel)
+    assert not np.isnan(as_f64(res.residual_out, case.act_dtype)).any()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_mixed_shared_and_missing_scales(kernel):
+    case = synth.make_case("mix", T=7, H=1536, K=6, R=4, E=32, rsf=2.5, shared=True)
+    case.shared[1] = None
+    case.shared[3] = None
+    case.scale[2] = None
+    check_case(case, kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("act", [torch.float16, torch.bfloat16])
+def test_overflow_and_cancellation(kernel, act):
+    """Large rows that overflow fp16, and partials that cancel (the tight fixture asked for in the review
+    of flashinfer PR #6631: accumulation in FP32 must be visible in the result)."""
+    case = synth.make_case("big", T=4, H=512, K=8, R=4, E=16, act_dtype=act, rsf=2.5, shared=True,
+                           gemm2_std=3000.0 if act == torch.float16 else 1e30)
+    check_case(case, kernel)
+    c2 = synth.make_case("cancel", T=4, H=512, K=8, R=2, E=16, act_dtype=act, rsf=1.0)
+    c2.gemm2[1] = -c2.gemm2[0]
+    c2.perm[1] = c2.perm[0].clone()
+    c2.scale[1] = c2.scale[0].clone()
+    res, want = check_case(c2, kernel)
+    # p_1 = -p_0 exactly, so the routed sum is 0 and residual_out == residual
+    assert np.array_equal(res.residual_out, bits16(c2.residual))
+
+
+# --------------------------------------------------------------------------------------------
+# Launch modes
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_pdl_on_off_bitwise_equal_over_many_routings(kernel):
+    """flashinfer PR #6546, Description: outputs with PDL on are bitwise equal to PDL off over 900
+    routings (1-16 tokens, top-8).  Same here, also with the early routing read."""
+    n = 0
+    for seed in range(60):
+        for T in (1, 2, 5, 8, 13, 16):
+            case = on_gpu(synth.make_case("pdl", T=T, H=2048, K=8, R=2, E=64, rsf=2.5, shared=True,
+                                          seed_base=seed * 10_000))
+            a = run(case, kernel=kernel, pdl=True)
+            b = run(case, kernel=kernel, pdl=False)
+            c = run(case, kernel=kernel, pdl=True, routing_ready=True)
+            assert np.array_equal(a.residual_out, b.residual_out) and np.array_equal(a.norm_out, b.norm_out)
+            assert np.array_equal(a.residual_out, c.residual_out) and np.array_equal(a.norm_out, c.norm_out)
+            n += 1
+    assert n == 360
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_graph_replay_back_to_back(kernel):
+    """flashinfer PR #6631 (walkthrough): capture 20 back-to-back launches, replay 50 times, check that
+    it completes within 60 s and the result is right.  The deadline is a host loop on an event."""
+    import moe_finalize_residual_gb300 as mfr
+    case_cpu = synth.make_case("graph", T=64, H=6144, K=8, R=4, E=256, rsf=2.5, shared=True)
+    g = on_gpu(case_cpu)
+    ro = torch.empty_like(g.residual)
+    no = torch.empty_like(g.residual)
+    parts = partials_of(g)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            mfr.moe_finalize_fused(parts, g.residual, g.gamma, routed_scaling_factor=g.rsf, eps=g.eps,
+                                   residual_out=ro, norm_out=no, kernel=kernel)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(20):
+            mfr.moe_finalize_fused(parts, g.residual, g.gamma, routed_scaling_factor=g.rsf, eps=g.eps,
+                                   residual_out=ro, norm_out=no, kernel=kernel)
+    ro.zero_()
+    ev = torch.cuda.Event()
+    for _ in range(50):
+        graph.replay()
+    ev.record()
+    deadline = time.time() + 60
+    while not ev.query():
+        assert time.time() < deadline, "graph replay did not finish within 60 s"
+        time.sleep(0.001)
+    from helpers import Result
+    res = Result(bits16(ro), bits16(no), None, None, True)
+    check_against_oracle(case_cpu, res)
+
+
+def test_kernel_choice_and_plan():
+    import moe_finalize_residual_gb300 as mfr
+    small = on_gpu(synth.make_case("p", T=4, H=6144, K=8, R=4, E=64, shared=True))
+    big = synth.make_case("p", T=2048, H=6144, K=8, R=4, E=64, device="cuda")
+    p1 = mfr.moe_finalize_plan(partials_of(small), small.residual, small.gamma)
+    p2 = mfr.moe_finalize_plan(partials_of(big), big.residual, big.gamma)
+    assert p1["kernel"] == "cluster" and p1["cluster"] >= 2 and p1["grid"] == 4 * p1["cluster"]
+    assert p2["kernel"] == "stream" and p2["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count * 2
+
+
+def test_deterministic_repeats():
+    case = on_gpu(synth.make_case("det", T=33, H=4096, K=8, R=4, E=64, rsf=2.5, shared=True))
+    for kernel in KERNELS:
+        a = run(case, kernel=kernel)
+        for _ in range(3):
+            b = run(case, kernel=kernel)
+            assert np.array_equal(a.residual_out, b.residual_out) and np.array_equal(a.norm_out, b.norm_out)
+
+
+def test_per_step_rounding_model_fails_parity():
+    """Negative control: the old kernel's numerics (every step rounded to the activation type, as the
+    pages describe) must not pass the parity check, so the check can tell the two apart."""
+    case = synth.make_p1_case(8, 6144)
+    res = run(on_gpu(case), kernel="cluster")
+    stock = oracle.finalize(case, mode=oracle.MODE_STEP_ROUNDED)
+    with pytest.raises(AssertionError):
+        check_against_oracle(case, res, want=stock)
+    check_against_oracle(case, res)
+
+
+def test_invalid_arguments_write_nothing():
+    import moe_finalize_residual_gb300 as mfr
+    case = on_gpu(synth.make_case("bad", T=4, H=256, K=2, R=1, E=8))
+    out = Guarded(4 * 256 * 2, "cuda", torch.bfloat16, (4, 256))
+    parts = partials_of(case)
+    with pytest.raises(mfr.MoEFinalizeError, match="sf_out"):
+        _call_without_sf(mfr, parts, case, out)
+    with pytest.raises(ValueError):
+        mfr.moe_finalize_fused(parts, case.residual.cpu(), case.gamma, residual_out=out.view)
+    torch.cuda.synchronize()
+    assert out.guards_intact() and np.all(out.payload() == CANARY)
+
+
+def _call_without_sf(mfr, parts, case, out):
+    import ctypes
+    a, keep = mfr._build_args(parts, case.residual, case.gamma, 1.0, 1e-6, out.view, None, 2,
+                              torch.ones(1, device="cuda"), 0, torch.empty(512, dtype=torch.uint8, device="cuda"),
+                              None, 1, 0, check=False)
+    mfr._check(mfr.raw_library().moe_finalize_fused(ctypes.byref(a), None))
+
+
+def test_no_wait_timed_out():
+    import moe_finalize_residual_gb300 as mfr
+    assert mfr.moe_finalize_read_timeouts() == 0
