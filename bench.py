@@ -187,11 +187,11 @@ def traffic_for(kernel_name: str):
         return None
     try:
         d = json.load(open(p))
-        from moe_finalize_residual_gb300 import build as b
         import hashlib
+        csrc = os.path.join(ROOT, "moe_finalize_residual_gb300", "csrc")
         h = hashlib.sha256()
-        for name in sorted(os.listdir(b.CSRC)):
-            h.update(open(os.path.join(b.CSRC, name), "rb").read())
+        for name in sorted(os.listdir(csrc)):
+            h.update(open(os.path.join(csrc, name), "rb").read())
         e = d.get(kernel_name)
         if e and e.get("source_sha256") == h.hexdigest():
             return e["dram_bytes_per_launch"]

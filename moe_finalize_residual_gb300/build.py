@@ -7,6 +7,7 @@ from __future__ import annotations
 
 import concurrent.futures
 import os
+import platform
 import shutil
 import subprocess
 
@@ -44,6 +45,12 @@ def _stale(obj: str, src: str) -> bool:
 def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) -> str:
     """Compile (only what changed, unless ``force``) and link.  Returns the library path."""
     os.makedirs(BUILD, exist_ok=True)
+    stamp = os.path.join(BUILD, "MACHINE")
+    machine = platform.machine()
+    if not os.path.exists(stamp) or open(stamp).read().strip() != machine:
+        force = True  # objects from another architecture must not be linked here
+        with open(stamp, "w") as f:
+            f.write(machine + "\n")
     jobs = []
     for name in SOURCES:
         src = os.path.join(CSRC, name)

@@ -18,8 +18,9 @@ HEADER = os.path.join(ROOT, "include", "moe_finalize.h")
 
 @pytest.fixture(scope="module")
 def mfr():
-    from moe_finalize_residual_gb300 import build as b
-    b.build()
+    sys.path.insert(0, ROOT)
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import moe_finalize_residual_gb300 as m
     return m
 
