@@ -170,8 +170,15 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
   const int nvec = a->H / 8;
   const int unit = (a->H % 16 == 0) ? 2 : 1;  // slices start on 16-element blocks when H allows
   const int ns = p->nslots;
-  const int c0 = std::min(kMaxCluster, pow2_ceil(ceil_div(2 * d.sms, std::max(1, a->T))));
-  for (int C = c0; C <= kMaxCluster; C *= 2) {
+  // Preferred cluster size: enough CTAs to cover the GPU twice; then larger sizes (smaller slices, less
+  // shared memory each), then smaller ones.  Every CTA must get at least one unit of the hidden size.
+  const int max_c = std::min(kMaxCluster, std::max(1, nvec / unit));
+  const int c0 = std::min(max_c, pow2_ceil(ceil_div(2 * d.sms, std::max(1, a->T))));
+  int cands[16], nc = 0;
+  for (int C = c0; C <= max_c; C *= 2) cands[nc++] = C;
+  for (int C = c0 / 2; C >= 1; C /= 2) cands[nc++] = C;
+  for (int ci = 0; ci < nc; ++ci) {
+    const int C = cands[ci];
     const int slice_vec = align_up(ceil_div(nvec, C), unit);
     if ((C - 1) * slice_vec >= nvec && C > 1) continue;  // a CTA would get no hidden elements
     const int block = std::max(64, align_up(ceil_div(slice_vec * 8, 4), 32));
