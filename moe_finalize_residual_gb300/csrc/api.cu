@@ -161,8 +161,18 @@ int pow2_ceil(int x) {
   return p;
 }
 
-// Token count up to which the cluster kernel is chosen automatically.
-constexpr int kClusterMaxTokens = 256;
+// Token count up to which the cluster kernel is chosen automatically, and the stream kernel's shape
+// (probe builds may override them).
+#ifndef MFR_CLUSTER_MAX_TOKENS
+#define MFR_CLUSTER_MAX_TOKENS 256
+#endif
+#ifndef MFR_STREAM_CONSUMER_WARPS
+#define MFR_STREAM_CONSUMER_WARPS 4
+#endif
+#ifndef MFR_STREAM_STAGES
+#define MFR_STREAM_STAGES 4
+#endif
+constexpr int kClusterMaxTokens = MFR_CLUSTER_MAX_TOKENS;
 constexpr int kMaxCluster = 16;
 
 // Cluster kernel: C CTAs per token, each holding every row of its hidden slice in shared memory.
@@ -182,10 +192,12 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
     const int slice_vec = align_up(ceil_div(nvec, C), unit);
     if ((C - 1) * slice_vec >= nvec && C > 1) continue;  // a CTA would get no hidden elements
     const int block = std::max(64, align_up(ceil_div(slice_vec * 8, 4), 32));
-    const int off_src = align_up(ns * slice_vec * 16, 16);
-    const int off_scale = off_src + ns * 8;
-    const int off_flag = off_scale + ns * 4;
-    const int off_red = align_up(off_flag + ns, 16);
+    const int stride = slice_vec * 16;
+    const int off_zero = align_up(ns * stride, 16);
+    const int off_src = off_zero + stride;
+    const int off_meta = off_src + ns * 8;
+    const int off_shoff = off_meta + a->R * a->K * 8;
+    const int off_red = align_up(off_shoff + MFR_MAX_PARTIALS * 4, 16);
     const int smem = align_up(off_red + 34 * 4, 128);
     if (block > 1024 || smem > d.smem_optin) continue;
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
@@ -205,9 +217,10 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
       if (n < 1) continue;
     }
     p->slice_vec = slice_vec;
+    p->off_zero = off_zero;
     p->off_src = off_src;
-    p->off_scale = off_scale;
-    p->off_flag = off_flag;
+    p->off_meta = off_meta;
+    p->off_shoff = off_shoff;
     p->off_red = off_red;
     *g = geo;
     return true;
@@ -217,19 +230,20 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
 
 // Stream kernel: persistent CTAs, hidden streamed in chunks through a stage ring.
 bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
-  const int ncw = 4;
+  const int ncw = MFR_STREAM_CONSUMER_WARPS;
   const int block = 32 * (2 + ncw);
   const int ns = p->nslots;
   const int D = 4;
-  const int ring_bytes = align_up(((ns * 13 + 3) & ~3) + 4, 16);
+  const int ring_bytes = align_up(ns * 8 + a->R * a->K * 8 + MFR_MAX_PARTIALS * 4 + 4, 16);
   for (int CH = 128 * ncw; CH >= 64; CH /= 2) {
     const int ch = std::min(CH, align_up(a->H, 16));
     const int stage_bytes = (ns + 1) * ch * 2;
-    for (int NS = 4; NS >= 2; --NS) {
+    for (int NS = MFR_STREAM_STAGES; NS >= 2; --NS) {
       const int bar_bytes = 8 * (2 * NS + 2 * D + 3) + 8;
       const int off_stage = align_up(bar_bytes, 128);
       const int off_ring = off_stage + NS * stage_bytes;
-      const int off_gamma = align_up(off_ring + D * ring_bytes, 16);
+      const int off_zero = align_up(off_ring + D * ring_bytes, 16);
+      const int off_gamma = off_zero + ch * 2;
       const int off_stash = off_gamma + align_up(a->H * 2, 16);
       const int off_sred = off_stash + align_up(a->H * 2, 16);
       const int smem = align_up(off_sred + 2 * 32 * 4, 128);
@@ -257,6 +271,7 @@ bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, La
       p->off_bar = 0;
       p->off_stage = off_stage;
       p->off_ring = off_ring;
+      p->off_zero_s = off_zero;
       p->off_gamma = off_gamma;
       p->off_stash = off_stash;
       p->off_sred = off_sred;

@@ -26,7 +26,23 @@
 
 namespace mfr {
 
-template <typename A>
+// Build this CTA's slot table for token t: the global source of every staged row, and the
+// (offset, scale) table the arithmetic reads.  Slot s is staged at byte s * stride.
+__device__ __forceinline__ void load_slots(const KParams& p, int t, int stride, const uint8_t** slot_src,
+                                           int2* meta, int* sh_off, int tid, int nthreads) {
+  for (int s = tid; s < p.nslots; s += nthreads) {
+    const SlotSource o = slot_source(p, s, t);
+    slot_src[s] = o.src;
+    if (o.k >= 0)
+      meta[o.r * p.K + o.k] = make_int2(o.src ? s * stride : -1, __float_as_int(o.scale));
+    else
+      sh_off[o.r] = s * stride;
+  }
+  for (int r = tid; r < p.R; r += nthreads)
+    if (!((p.shared_mask >> r) & 1u)) sh_off[r] = -1;
+}
+
+template <typename A, int RMAX>
 __global__ void __launch_bounds__(1024, 1) cluster_finalize_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -38,33 +54,21 @@ __global__ void __launch_bounds__(1024, 1) cluster_finalize_kernel(const __grid_
   const int nvec_total = H >> 3;
   const int v0 = static_cast<int>(crank) * p.slice_vec;
   const int nv = max(0, min(nvec_total - v0, p.slice_vec));  // 16-byte vectors of this CTA's slice
-  const int slice_elems = p.slice_vec * 8;                   // stage row stride
+  const int stride = p.slice_vec * 16;                       // bytes per staged row
   const int nslots = p.nslots;
 
-  uint8_t* stage = smem;  // [nslots][slice_elems] act
+  uint8_t* stage = smem;  // [nslots][slice] act
+  uint8_t* zero_row = smem + p.off_zero;
   const uint8_t** slot_src = reinterpret_cast<const uint8_t**>(smem + p.off_src);
-  float* slot_scale = reinterpret_cast<float*>(smem + p.off_scale);
-  uint8_t* slot_flag = smem + p.off_flag;
+  int2* meta = reinterpret_cast<int2*>(smem + p.off_meta);
+  int* sh_off = reinterpret_cast<int*>(smem + p.off_shoff);
   float* red = reinterpret_cast<float*>(smem + p.off_red);  // [32] warp sums, [32] CTA sum, [33] total
 
+  for (int i = tid; i < p.slice_vec; i += nthreads) reinterpret_cast<uint4*>(zero_row)[i] = make_uint4(0, 0, 0, 0);
   if (p.pdl) pdl_launch_dependents();
-  if (p.routing_early) {
-    for (int s = tid; s < nslots; s += nthreads) {
-      const SlotInfo si = slot_info(p, s, t);
-      slot_src[s] = si.src;
-      slot_scale[s] = si.scale;
-      slot_flag[s] = static_cast<uint8_t>(si.flags);
-    }
-  }
+  if (p.routing_early) load_slots(p, t, stride, slot_src, meta, sh_off, tid, nthreads);
   if (p.pdl) pdl_wait();
-  if (!p.routing_early) {
-    for (int s = tid; s < nslots; s += nthreads) {
-      const SlotInfo si = slot_info(p, s, t);
-      slot_src[s] = si.src;
-      slot_scale[s] = si.scale;
-      slot_flag[s] = static_cast<uint8_t>(si.flags);
-    }
-  }
+  if (!p.routing_early) load_slots(p, t, stride, slot_src, meta, sh_off, tid, nthreads);
   __syncthreads();
 
   // Gather: every valid (slot, 16-byte vector) pair of this slice, all in flight together.
@@ -75,8 +79,7 @@ __global__ void __launch_bounds__(1024, 1) cluster_finalize_kernel(const __grid_
     const int v = i - s * nv;
     const uint8_t* src = slot_src[s];
     if (src != nullptr)
-      cp_async16(stage_addr + (static_cast<uint32_t>(s) * slice_elems + v * 8) * 2,
-                 src + static_cast<int64_t>(v0 + v) * 16);
+      cp_async16(stage_addr + static_cast<uint32_t>(s) * stride + v * 16, src + static_cast<int64_t>(v0 + v) * 16);
   }
   cp_async_commit();
 
@@ -92,16 +95,10 @@ __global__ void __launch_bounds__(1024, 1) cluster_finalize_kernel(const __grid_
   cp_async_wait_all();
   __syncthreads();
 
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, S[4] = {0.f, 0.f, 0.f, 0.f}, x[4] = {0.f, 0.f, 0.f, 0.f};
+  float S[4] = {0.f, 0.f, 0.f, 0.f}, x[4] = {0.f, 0.f, 0.f, 0.f};
   float ss = 0.0f;
   if (active) {
-    const uint8_t* col = stage + static_cast<int64_t>(el) * 2;
-    for (int s = 0; s < nslots; ++s) {
-      const uint32_t f = slot_flag[s];
-      uint2 row = make_uint2(0, 0);
-      if (f & kValid) row = *reinterpret_cast<const uint2*>(col + static_cast<int64_t>(s) * slice_elems * 2);
-      finalize_step<A>(f, slot_scale[s], row, p.rsf, acc, S);
-    }
+    finalize4<A, RMAX>(meta, sh_off, stage, zero_row, el * 2, p.R, p.K, p.rsf, S);
     const uint2 ro = residual_step<A>(S, res_raw, x, ss);
     if (p.residual_out != nullptr) stg8(p.residual_out + (static_cast<int64_t>(t) * H + h) * 2, ro);
   }
@@ -135,9 +132,9 @@ __global__ void __launch_bounds__(1024, 1) cluster_finalize_kernel(const __grid_
   if (C > 1) cluster_wait_acquire();  // no CTA leaves while a peer may still read its shared memory
 }
 
-template <typename A>
+template <typename A, int RMAX>
 static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  auto kern = cluster_finalize_kernel<A>;
+  auto kern = cluster_finalize_kernel<A, RMAX>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -170,9 +167,9 @@ static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStr
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <typename A>
+template <typename A, int RMAX>
 static int max_active_clusters(const LaunchGeom& g) {
-  auto kern = cluster_finalize_kernel<A>;
+  auto kern = cluster_finalize_kernel<A, RMAX>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaLaunchConfig_t cfg = {};
@@ -194,12 +191,22 @@ static int max_active_clusters(const LaunchGeom& g) {
   return n;
 }
 
-cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  return act_dtype == MFR_BF16 ? launch_cluster<__nv_bfloat16>(p, g, stream) : launch_cluster<__half>(p, g, stream);
+template <typename A>
+static cudaError_t launch_cluster_r(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
+  if (p.R <= 1) return launch_cluster<A, 1>(p, g, stream);
+  if (p.R <= 2) return launch_cluster<A, 2>(p, g, stream);
+  if (p.R <= 4) return launch_cluster<A, 4>(p, g, stream);
+  return launch_cluster<A, 8>(p, g, stream);
 }
 
+cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
+  return act_dtype == MFR_BF16 ? launch_cluster_r<__nv_bfloat16>(p, g, stream) : launch_cluster_r<__half>(p, g, stream);
+}
+
+// Occupancy of the cluster kernel; the R bound does not change its resources materially, so the
+// widest instantiation answers for all.
 int cluster_kernel_max_active_clusters(int act_dtype, const LaunchGeom& g) {
-  return act_dtype == MFR_BF16 ? max_active_clusters<__nv_bfloat16>(g) : max_active_clusters<__half>(g);
+  return act_dtype == MFR_BF16 ? max_active_clusters<__nv_bfloat16, 8>(g) : max_active_clusters<__half, 8>(g);
 }
 
 }  // namespace mfr

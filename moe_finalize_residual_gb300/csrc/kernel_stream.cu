@@ -57,7 +57,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag));
 }
 
-template <typename A>
+template <typename A, int RMAX>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -76,14 +76,18 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * NS + 2 * D + 3);
   uint8_t* stage0 = smem + p.off_stage;
   uint8_t* ring0 = smem + p.off_ring;
+  uint8_t* zero_row = smem + p.off_zero_s;
   uint8_t* gamma_s = smem + p.off_gamma;
   uint8_t* stash = smem + p.off_stash;
   float* sred = reinterpret_cast<float*>(smem + p.off_sred);  // [2][32]
 
-  // Routing ring entry layout: row address [nslots] | scale [nslots] | flags [nslots] | valid count.
-  const int ring_off_scale = nslots * 8;
-  const int ring_off_flag = ring_off_scale + nslots * 4;
-  const int ring_off_count = (ring_off_flag + nslots + 3) & ~3;
+  // Routing ring entry: row address [nslots] | (offset, scale) [R*K] | shared offset [8] | valid count.
+  // Offsets are relative to a stage's base: slot s sits at s * CH * 2, the residual at nslots * CH * 2.
+  const int ring_off_meta = nslots * 8;
+  const int ring_off_shoff = ring_off_meta + p.R * p.K * 8;
+  const int ring_off_count = ring_off_shoff + MFR_MAX_PARTIALS * 4;
+
+  for (int i = tid; i < CH / 8; i += blockDim.x) reinterpret_cast<uint4*>(zero_row)[i] = make_uint4(0, 0, 0, 0);
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -117,12 +121,16 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
       uint8_t* e = ring0 + slot * p.ring_bytes;
       int nvalid = 0;
       for (int s = lane; s < nslots; s += 32) {
-        const SlotInfo si = slot_info(p, s, t);
-        reinterpret_cast<const uint8_t**>(e)[s] = si.src;
-        reinterpret_cast<float*>(e + ring_off_scale)[s] = si.scale;
-        e[ring_off_flag + s] = static_cast<uint8_t>(si.flags);
-        nvalid += (si.flags & kValid) ? 1 : 0;
+        const SlotSource o = slot_source(p, s, t);
+        reinterpret_cast<const uint8_t**>(e)[s] = o.src;
+        if (o.k >= 0)
+          reinterpret_cast<int2*>(e + ring_off_meta)[o.r * p.K + o.k] =
+              make_int2(o.src ? s * CH * 2 : -1, __float_as_int(o.scale));
+        else
+          reinterpret_cast<int*>(e + ring_off_shoff)[o.r] = s * CH * 2;
+        nvalid += o.src ? 1 : 0;
       }
+      if (lane < p.R && !((p.shared_mask >> lane) & 1u)) reinterpret_cast<int*>(e + ring_off_shoff)[lane] = -1;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) nvalid += __shfl_xor_sync(0xffffffffu, nvalid, o);
       if (lane == 0) *reinterpret_cast<int*>(e + ring_off_count) = nvalid;
@@ -195,8 +203,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
       const uint32_t ph = static_cast<uint32_t>(i / D) & 1u;
       if (!warp_wait(rfull0 + 8u * slot, ph, abort_flag)) break;
       const uint8_t* e = ring0 + slot * p.ring_bytes;
-      const float* scales = reinterpret_cast<const float*>(e + ring_off_scale);
-      const uint8_t* flags = e + ring_off_flag;
+      const int2* meta = reinterpret_cast<const int2*>(e + ring_off_meta);
+      const int* sh_off = reinterpret_cast<const int*>(e + ring_off_shoff);
       float ss = 0.0f;
       bool ok = true;
       for (int c = 0; c < nch; ++c) {
@@ -209,15 +217,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
         const uint8_t* sb = stage0 + st * p.stage_bytes;
         const int el = j * 4;
         if (el < w) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f}, S[4] = {0.f, 0.f, 0.f, 0.f}, x[4];
-          const uint8_t* col = sb + static_cast<int64_t>(el) * 2;
-          for (int s = 0; s < nslots; ++s) {
-            const uint32_t f = flags[s];
-            uint2 row = make_uint2(0, 0);
-            if (f & kValid) row = *reinterpret_cast<const uint2*>(col + static_cast<int64_t>(s) * CH * 2);
-            finalize_step<A>(f, scales[s], row, p.rsf, acc, S);
-          }
-          const uint2 res_raw = *reinterpret_cast<const uint2*>(col + static_cast<int64_t>(nslots) * CH * 2);
+          float S[4] = {0.f, 0.f, 0.f, 0.f}, x[4];
+          finalize4<A, RMAX>(meta, sh_off, sb, zero_row, el * 2, p.R, p.K, p.rsf, S);
+          const uint2 res_raw = *reinterpret_cast<const uint2*>(sb + static_cast<int64_t>(nslots) * CH * 2 + el * 2);
           const uint2 ro = residual_step<A>(S, res_raw, x, ss);
           *reinterpret_cast<uint2*>(stash + static_cast<int64_t>(h0 + el) * 2) = ro;
           if (p.residual_out != nullptr) stg8(p.residual_out + (static_cast<int64_t>(t) * H + h0 + el) * 2, ro);
@@ -265,9 +267,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
   __syncthreads();
 }
 
-template <typename A>
+template <typename A, int RMAX>
 static cudaError_t launch_stream(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  auto kern = stream_finalize_kernel<A>;
+  auto kern = stream_finalize_kernel<A, RMAX>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -293,13 +295,21 @@ static cudaError_t launch_stream(const KParams& p, const LaunchGeom& g, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <typename A>
+static cudaError_t launch_stream_r(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
+  if (p.R <= 1) return launch_stream<A, 1>(p, g, stream);
+  if (p.R <= 2) return launch_stream<A, 2>(p, g, stream);
+  if (p.R <= 4) return launch_stream<A, 4>(p, g, stream);
+  return launch_stream<A, 8>(p, g, stream);
+}
+
 cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  return act_dtype == MFR_BF16 ? launch_stream<__nv_bfloat16>(p, g, stream) : launch_stream<__half>(p, g, stream);
+  return act_dtype == MFR_BF16 ? launch_stream_r<__nv_bfloat16>(p, g, stream) : launch_stream_r<__half>(p, g, stream);
 }
 
 template <typename A>
 static int blocks_per_sm(const LaunchGeom& g) {
-  auto kern = stream_finalize_kernel<A>;
+  auto kern = stream_finalize_kernel<A, 8>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, g.block, g.smem) != cudaSuccess) {

@@ -55,20 +55,15 @@ struct KParams {
   float rsf, eps;
   // cluster kernel
   int32_t slice_vec;      // 16-byte vectors of hidden per CTA (the last CTA may hold fewer)
-  int32_t off_src, off_scale, off_flag, off_red;
+  int32_t off_zero, off_src, off_meta, off_shoff, off_red;
   // stream kernel
   int32_t chunk;          // hidden elements per pipeline stage
   int32_t stages;         // pipeline depth
   int32_t rdepth;         // routing ring depth (tokens)
   int32_t stage_bytes;    // bytes of one stage: (nslots + 1 residual) * chunk * 2
   int32_t ring_bytes;     // bytes of one routing ring entry
-  int32_t off_bar, off_stage, off_ring, off_gamma, off_stash, off_sred;
+  int32_t off_bar, off_stage, off_ring, off_zero_s, off_gamma, off_stash, off_sred;
 };
-
-// Slot flags.
-constexpr uint32_t kValid = 1u;   // the row exists (route index in range, or a shared row)
-constexpr uint32_t kEnd = 2u;     // last slot of its partial: scale, round and add to the rank sum
-constexpr uint32_t kShared = 4u;  // the shared-expert row of its partial
 
 // ------------------------------------------------------------------------------------------------
 // PTX wrappers
@@ -219,68 +214,93 @@ __device__ __forceinline__ float load_scale(const void* base, int64_t i, int dty
 }
 
 // ------------------------------------------------------------------------------------------------
-// Routing metadata: one "slot" per row a token may read.  Slots are ordered partial by partial;
-// within a partial, routes k = 0..K-1 and then the shared-expert row (if any).
+// Routing metadata.  Every row a token may read is a "slot": routes are slots r*K + k, the shared
+// rows of the partials that have one follow as slots R*K + 0, 1, ...  A kernel stages slot s at byte
+// offset s * stride of its stage and describes the token by a table:
+//   meta[r*K + k] = {byte offset of the route's row in the stage, or -1 if the route is skipped;
+//                    bits of its FP32 scale, or of -0.0f if skipped}
+//   sh_off[r]     = byte offset of partial r's shared row, or -1.
+// A skipped route reads a row of zeros with scale -0.0: fma(-0.0, +0.0, acc) == acc for every acc
+// (including -0, infinities and NaN), so skipping costs no branch and changes no bit.
 // ------------------------------------------------------------------------------------------------
 
-struct SlotInfo {
-  const uint8_t* src;  // start of the row (hidden index 0), nullptr if the route is skipped
+__device__ __forceinline__ int shared_slot(const KParams& p, int r) {
+  return p.R * p.K + __popc(p.shared_mask & ((1u << r) - 1u));
+}
+
+struct SlotSource {
+  const uint8_t* src;  // row start in global memory (hidden index 0); nullptr if skipped
   float scale;
-  uint32_t flags;
+  int r, k;            // partial and route (k == -1 for a shared row)
 };
 
 // flashinfer PR #6631, Test changes: routes set to -1 contribute nothing; one bound check per route.
-__device__ __forceinline__ SlotInfo slot_info(const KParams& p, int s, int t) {
-  int r = 0, base = 0;
-  for (; r < p.R; ++r) {
-    const int n = p.K + static_cast<int>((p.shared_mask >> r) & 1u);
-    if (s < base + n) break;
-    base += n;
+__device__ __forceinline__ SlotSource slot_source(const KParams& p, int s, int t) {
+  SlotSource o;
+  if (s < p.R * p.K) {
+    o.r = s / p.K;
+    o.k = s - o.r * p.K;
+    const KPartial& P = p.part[o.r];
+    const int64_t e = static_cast<int64_t>(t) * p.K + o.k;
+    const int32_t idx = P.perm[e];
+    const bool valid = idx >= 0 && static_cast<int64_t>(idx) < P.rows;
+    o.src = valid ? P.gemm2 + static_cast<int64_t>(idx) * p.H * 2 : nullptr;
+    o.scale = valid ? load_scale(P.scale, e, p.scale_dtype) : -0.0f;
+  } else {
+    int j = s - p.R * p.K;  // j-th partial with a shared row
+    uint32_t m = p.shared_mask;
+    for (; j > 0; --j) m &= m - 1u;
+    o.r = __ffs(m) - 1;
+    o.k = -1;
+    o.src = p.part[o.r].shared + static_cast<int64_t>(t) * p.H * 2;
+    o.scale = 1.0f;
   }
-  const int k = s - base;
-  const KPartial& P = p.part[r];
-  const bool has_shared = (p.shared_mask >> r) & 1u;
-  SlotInfo si;
-  if (k == p.K) {  // the shared-expert row
-    si.src = P.shared + static_cast<int64_t>(t) * p.H * 2;
-    si.scale = 1.0f;
-    si.flags = kValid | kEnd | kShared;
-    return si;
-  }
-  const int64_t e = static_cast<int64_t>(t) * p.K + k;
-  const int32_t idx = P.perm[e];
-  const bool valid = idx >= 0 && static_cast<int64_t>(idx) < P.rows;
-  si.src = valid ? P.gemm2 + static_cast<int64_t>(idx) * p.H * 2 : nullptr;
-  si.scale = load_scale(P.scale, e, p.scale_dtype);
-  si.flags = (valid ? kValid : 0u) | ((k == p.K - 1 && !has_shared) ? kEnd : 0u);
-  return si;
+  return o;
 }
 
-// One step of the finalize for 4 consecutive elements: `row` is the slot's data, acc the partial's
-// FP32 accumulator, S the FP32 rank sum.
-template <typename A>
-__device__ __forceinline__ void finalize_step(uint32_t flags, float scale, uint2 row, float rsf, float acc[4],
-                                              float S[4]) {
-  if (flags & kValid) {
-    float v[4];
-    unpack4<A>(row, v);
-    if (flags & kShared) {
+// Finalize 4 consecutive elements (byte column `col` of every staged row): for each partial the FP32
+// fused multiply-add chain over its routes in order k = 0..K-1 starting from +0, times the routed
+// scaling factor, plus the shared row, rounded once to act; the rounded partials are added to S in
+// rank order 0..R-1 (flashinfer PR #6631, Description; TensorRT-LLM PR #16778, Fix; flashinfer PR
+// #3385, fixed rank order).  The R chains are independent until the rank sum, so they advance
+// together, route by route, which gives each thread 4*R independent FMA chains.
+template <typename A, int RMAX>
+__device__ __forceinline__ void finalize4(const int2* __restrict__ meta, const int* __restrict__ sh_off,
+                                          const uint8_t* stage, const uint8_t* zero_row, int col, int R, int K,
+                                          float rsf, float S[4]) {
+  float acc[RMAX][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = __fadd_rn(__fmul_rn(acc[i], rsf), v[i]);
-    } else {
+  for (int r = 0; r < RMAX; ++r) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = __fmaf_rn(scale, v[i], acc[i]);
+    for (int i = 0; i < 4; ++i) acc[r][i] = 0.0f;
+  }
+#pragma unroll 2
+  for (int k = 0; k < K; ++k) {
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      if (r < R) {
+        const int2 m = meta[r * K + k];
+        const uint8_t* row = (m.x >= 0) ? stage + m.x : zero_row;
+        float v[4];
+        unpack4<A>(*reinterpret_cast<const uint2*>(row + col), v);
+        const float sc = __int_as_float(m.y);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[r][i] = __fmaf_rn(sc, v[i], acc[r][i]);
+      }
     }
   }
-  if (flags & kEnd) {
-    if (!(flags & kShared)) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = __fmul_rn(acc[i], rsf);
-    }
+  for (int r = 0; r < RMAX; ++r) {
+    if (r < R) {
+      const int so = sh_off[r];
+      float sh[4] = {0.f, 0.f, 0.f, 0.f};
+      if (so >= 0) unpack4<A>(*reinterpret_cast<const uint2*>(stage + so + col), sh);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      S[i] = __fadd_rn(S[i], Act<A>::round(acc[i]));  // p_r rounded once, summed in FP32 in rank order
-      acc[i] = 0.0f;
+      for (int i = 0; i < 4; ++i) {
+        float a = __fmul_rn(acc[r][i], rsf);
+        if (so >= 0) a = __fadd_rn(a, sh[i]);
+        S[i] = __fadd_rn(S[i], Act<A>::round(a));  // p_r rounded once, summed in FP32 in rank order
+      }
     }
   }
 }
