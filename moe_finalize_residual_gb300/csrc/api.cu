@@ -166,43 +166,39 @@ int pow2_ceil(int x) {
 #ifndef MFR_CLUSTER_MAX_TOKENS
 #define MFR_CLUSTER_MAX_TOKENS 256
 #endif
-#ifndef MFR_STREAM_CONSUMER_WARPS
-#define MFR_STREAM_CONSUMER_WARPS 4
+#ifndef MFR_CLUSTER_BLOCK
+#define MFR_CLUSTER_BLOCK 512
 #endif
-#ifndef MFR_STREAM_STAGES
-#define MFR_STREAM_STAGES 4
+#ifndef MFR_STREAM_CONSUMER_WARPS
+#define MFR_STREAM_CONSUMER_WARPS 16
 #endif
 constexpr int kClusterMaxTokens = MFR_CLUSTER_MAX_TOKENS;
 constexpr int kMaxCluster = 16;
 
-// Cluster kernel: C CTAs per token, each holding every row of its hidden slice in shared memory.
+// Cluster kernel: C CTAs per token, each holding SV 16-byte vectors of the hidden row for all R
+// partials (R*SV threads).  SV comes from the parallelism target (about two CTAs per SM over the batch),
+// capped by the preferred CTA size, and bounded so that C <= 16 and R*SV <= kClusterMaxThreads.
 bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
   const int nvec = a->H / 8;
   const int unit = (a->H % 16 == 0) ? 2 : 1;  // slices start on 16-element blocks when H allows
-  const int ns = p->nslots;
-  // Preferred cluster size: enough CTAs to cover the GPU twice; then larger sizes (smaller slices, less
-  // shared memory each), then smaller ones.  Every CTA must get at least one unit of the hidden size.
-  const int max_c = std::min(kMaxCluster, std::max(1, nvec / unit));
-  const int c0 = std::min(max_c, pow2_ceil(ceil_div(2 * d.sms, std::max(1, a->T))));
-  int cands[16], nc = 0;
-  for (int C = c0; C <= max_c; C *= 2) cands[nc++] = C;
-  for (int C = c0 / 2; C >= 1; C /= 2) cands[nc++] = C;
-  for (int ci = 0; ci < nc; ++ci) {
-    const int C = cands[ci];
-    const int slice_vec = align_up(ceil_div(nvec, C), unit);
-    if ((C - 1) * slice_vec >= nvec && C > 1) continue;  // a CTA would get no hidden elements
-    const int block = std::max(64, align_up(ceil_div(slice_vec * 8, 4), 32));
-    const int stride = slice_vec * 16;
-    const int off_zero = align_up(ns * stride, 16);
-    const int off_src = off_zero + stride;
-    const int off_meta = off_src + ns * 8;
-    const int off_shoff = off_meta + a->R * a->K * 8;
-    const int off_red = align_up(off_shoff + MFR_MAX_PARTIALS * 4, 16);
-    const int smem = align_up(off_red + 34 * 4, 128);
-    if (block > 1024 || smem > d.smem_optin) continue;
+  const int R = a->R;
+  const int sv_max = (kClusterMaxThreads / R) / unit * unit;
+  const int sv_min = align_up(ceil_div(nvec, kMaxCluster), unit);
+  if (sv_min > sv_max) return false;
+  const int c_target = std::min(kMaxCluster, pow2_ceil(ceil_div(2 * d.sms, std::max(1, a->T))));
+  const int sv_soft = std::max(unit, (MFR_CLUSTER_BLOCK / R) / unit * unit);
+  int sv = align_up(ceil_div(nvec, c_target), unit);
+  sv = std::min(sv, std::max(sv_soft, sv_min));
+  sv = std::min(std::max(sv, sv_min), sv_max);
+  for (; sv <= sv_max; sv = std::min(sv_max + unit, align_up(sv * 2, unit))) {
+    const int C = ceil_div(nvec, sv);
+    const int block = align_up(sv * R, 32);
+    const int off_red = align_up((R + 2) * sv * 16, 16);
+    const int smem = align_up(off_red + 34 * 4, 16);
+    if (smem > d.smem_optin) continue;
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
     if (C > 1) {
-      const auto key = std::make_tuple(dev, a->act_dtype, C, block, smem);
+      const auto key = std::make_tuple(dev, a->act_dtype * 2 + (a->K > 8 ? 1 : 0), C, block, smem);
       int n;
       {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -210,17 +206,13 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
         n = (it == g_cluster_ok.end()) ? -1 : it->second;
       }
       if (n < 0) {
-        n = cluster_kernel_max_active_clusters(a->act_dtype, geo);
+        n = cluster_kernel_max_active_clusters(a->act_dtype, a->K, geo);
         std::lock_guard<std::mutex> lock(g_mu);
         g_cluster_ok[key] = n;
       }
       if (n < 1) continue;
     }
-    p->slice_vec = slice_vec;
-    p->off_zero = off_zero;
-    p->off_src = off_src;
-    p->off_meta = off_meta;
-    p->off_shoff = off_shoff;
+    p->slice_vec = sv;
     p->off_red = off_red;
     *g = geo;
     return true;
@@ -228,56 +220,53 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
   return false;
 }
 
-// Stream kernel: persistent CTAs, hidden streamed in chunks through a stage ring.
+// Stream kernel: persistent CTAs (one per SM), each compute thread copying its own 16-byte columns
+// of the rows ahead into a ring of kStreamSlots row slots.  A hidden pass is the widest multiple of
+// 8 * compute-threads elements (at most kStreamColumns per thread) for which the ring, gamma and the
+// kept residual row fit in shared memory.
 bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
   const int ncw = MFR_STREAM_CONSUMER_WARPS;
-  const int block = 32 * (2 + ncw);
-  const int ns = p->nslots;
-  const int D = 4;
-  const int ring_bytes = align_up(ns * 8 + a->R * a->K * 8 + MFR_MAX_PARTIALS * 4 + 4, 16);
-  for (int CH = 128 * ncw; CH >= 64; CH /= 2) {
-    const int ch = std::min(CH, align_up(a->H, 16));
-    const int stage_bytes = (ns + 1) * ch * 2;
-    for (int NS = MFR_STREAM_STAGES; NS >= 2; --NS) {
-      const int bar_bytes = 8 * (2 * NS + 2 * D + 3) + 8;
-      const int off_stage = align_up(bar_bytes, 128);
-      const int off_ring = off_stage + NS * stage_bytes;
-      const int off_zero = align_up(off_ring + D * ring_bytes, 16);
-      const int off_gamma = off_zero + ch * 2;
-      const int off_stash = off_gamma + align_up(a->H * 2, 16);
-      const int off_sred = off_stash + align_up(a->H * 2, 16);
-      const int smem = align_up(off_sred + 2 * 32 * 4, 128);
-      if (smem > d.smem_optin) continue;
-      LaunchGeom geo{0, block, 1, smem, d.smem_optin};
-      const auto key = std::make_tuple(dev, a->act_dtype, block, smem);
-      int bps;
-      {
-        std::lock_guard<std::mutex> lock(g_mu);
-        auto it = g_stream_bps.find(key);
-        bps = (it == g_stream_bps.end()) ? -1 : it->second;
-      }
-      if (bps < 0) {
-        bps = stream_kernel_blocks_per_sm(a->act_dtype, geo);
-        std::lock_guard<std::mutex> lock(g_mu);
-        g_stream_bps[key] = bps;
-      }
-      if (bps < 1) continue;
-      geo.grid = std::min(a->T, d.sms * bps);
-      p->chunk = ch;
-      p->stages = NS;
-      p->rdepth = D;
-      p->stage_bytes = stage_bytes;
-      p->ring_bytes = ring_bytes;
-      p->off_bar = 0;
-      p->off_stage = off_stage;
-      p->off_ring = off_ring;
-      p->off_zero_s = off_zero;
-      p->off_gamma = off_gamma;
-      p->off_stash = off_stash;
-      p->off_sred = off_sred;
-      *g = geo;
-      return true;
+  const int block = 32 * (1 + ncw);
+  const int step = 8 * 32 * ncw;
+  const int ring_bytes = align_up(16 + p->nslots * 16, 16);
+  const int bar_bytes = 8 * (2 * kStreamLists + 2) + 8;
+  const int off_stage = align_up(bar_bytes, 128);
+  for (int W = step * kStreamColumns; W >= step; W -= step) {
+    const int slot_bytes = std::min(W, a->H) * 2;
+    const int off_ring = off_stage + kStreamSlots * slot_bytes;
+    const int off_gamma = align_up(off_ring + kStreamLists * ring_bytes, 16);
+    const int off_stash = off_gamma + align_up(a->H * 2, 16);
+    const int off_sred = off_stash + align_up(a->H * 2, 16);
+    const int smem = align_up(off_sred + 2 * 32 * 4, 128);
+    if (smem > d.smem_optin) continue;
+    LaunchGeom geo{0, block, 1, smem, d.smem_optin};
+    const auto key = std::make_tuple(dev, a->act_dtype, block, smem);
+    int bps;
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      auto it = g_stream_bps.find(key);
+      bps = (it == g_stream_bps.end()) ? -1 : it->second;
     }
+    if (bps < 0) {
+      bps = stream_kernel_blocks_per_sm(a->act_dtype, geo);
+      std::lock_guard<std::mutex> lock(g_mu);
+      g_stream_bps[key] = bps;
+    }
+    if (bps < 1) continue;
+    geo.grid = std::min(a->T, d.sms * bps);
+    p->chunk = W;
+    p->stages = kStreamSlots;
+    p->rdepth = kStreamLists;
+    p->stage_bytes = slot_bytes;
+    p->ring_bytes = ring_bytes;
+    p->off_bar = 0;
+    p->off_stage = off_stage;
+    p->off_ring = off_ring;
+    p->off_gamma = off_gamma;
+    p->off_stash = off_stash;
+    p->off_sred = off_sred;
+    *g = geo;
+    return true;
   }
   return false;
 }
@@ -349,7 +338,7 @@ int moe_finalize_plan(const mfr_args* args, mfr_plan* plan) {
   plan->cluster = g.cluster;
   plan->block = g.block;
   plan->smem_bytes = g.smem;
-  plan->chunk = kernel == MFR_KERNEL_STREAM ? p.chunk : p.slice_vec * 8;
+  plan->chunk = kernel == MFR_KERNEL_STREAM ? p.chunk : p.slice_vec * 8;  // cluster: hidden elements per CTA
   plan->stages = kernel == MFR_KERNEL_STREAM ? p.stages : 1;
   return MFR_OK;
 }

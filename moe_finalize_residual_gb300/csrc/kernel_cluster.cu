@@ -2,105 +2,162 @@
 // equal slices, one slice per CTA of the cluster.
 //
 // Design (prior art: flashinfer PR #6546, finalizeKernelSmallBatch, Description -- one CTA per
-// (token, hidden slice), 128-bit loads, top-K split over thread groups with a shared-memory combine,
-// PDL trigger at kernel start; flashinfer PR #6631, Description -- load the indices and scales of
-// the routes first, then all rows, so the row loads are in flight together):
+// (token, hidden slice), 128-bit loads, top-K work split over thread groups combined through shared
+// memory, PDL trigger at kernel start; flashinfer PR #6631, Description -- load the indices and
+// scales of the routes first, then all rows, so the row loads are in flight together):
 //
-//  1. trigger dependents; read every slot's route index and scale into shared memory (before the
-//     dependency wait only when the caller says the routing is already complete);
-//  2. wait for the preceding kernel (PDL), then issue EVERY gathered row slice of EVERY partial as
-//     16-byte cp.async copies at once: all R*K routes and R shared rows of the token are in flight
-//     together, spread over all threads (this is the top-K split over thread groups);
-//  3. each thread owns 4 consecutive hidden elements and runs the FP32 fused multiply-add chain over
-//     the staged rows in route order (the shared-memory combine; the order is the definition's, so
-//     every partial's rounded row is bit-identical to a sequential evaluation);
-//  4. rank sum, residual add, sum of squares; the sum of squares is reduced with warp shuffles, then
-//     across warps in shared memory, then across the cluster's CTAs through distributed shared memory
-//     in CTA-rank order, so every CTA gets the same deterministic total;
-//  5. RMSNorm output and the quantisation epilogue.
+//  * a CTA holds SV 16-byte vectors of the token's hidden row; its threads form R groups of SV, one
+//    group per partial: thread (r, v) owns vector v of partial r;
+//  * each thread reads the route indices and scales of its partial (the same addresses for the whole
+//    warp), then issues all its rows as 128-bit loads at once (up to KC in flight; K > KC repeats),
+//    plus its shared-expert row, and runs the FP32 fused multiply-add chain over them in route order:
+//    every partial row is produced by one thread in the definition's order, so it is bit-exact;
+//  * each group writes its rounded partial row to shared memory; group 0 sums the R rows in rank order
+//    (the shared-memory combine), adds the residual and writes residual_out;
+//  * the sum of squares is reduced with warp shuffles, then across warps in shared memory, then across
+//    the cluster's CTAs through distributed shared memory in CTA-rank order, so every CTA gets the same
+//    deterministic total; group 0 then writes norm_out and the quantised output.
 //
-// No CTA waits on a flag in global memory; the only cross-CTA synchronisation is the hardware
-// cluster barrier, which every CTA reaches unconditionally.
+// No CTA waits on a flag in global memory; the only cross-CTA synchronisation is the hardware cluster
+// barrier, which every CTA reaches unconditionally.
 #include "mfr_device.cuh"
 #include "mfr_launch.h"
 
 namespace mfr {
 
-// Build this CTA's slot table for token t: the global source of every staged row, and the
-// (offset, scale) table the arithmetic reads.  Slot s is staged at byte s * stride.
-__device__ __forceinline__ void load_slots(const KParams& p, int t, int stride, const uint8_t** slot_src,
-                                           int2* meta, int* sh_off, int tid, int nthreads) {
-  for (int s = tid; s < p.nslots; s += nthreads) {
-    const SlotSource o = slot_source(p, s, t);
-    slot_src[s] = o.src;
-    if (o.k >= 0)
-      meta[o.r * p.K + o.k] = make_int2(o.src ? s * stride : -1, __float_as_int(o.scale));
-    else
-      sh_off[o.r] = s * stride;
+// Route indices and scales of routes k0..k0+KC-1 of partial P for token t; idx < 0 marks a route to
+// skip (flashinfer PR #6631, Test changes: -1 routes contribute nothing; one bound check per route).
+template <int KC>
+__device__ __forceinline__ void load_routes(const KParams& p, const KPartial& P, int t, int k0, bool on,
+                                            int idx[KC], float sc[KC]) {
+#pragma unroll
+  for (int j = 0; j < KC; ++j) {
+    idx[j] = -1;
+    sc[j] = 0.0f;
+    const int k = k0 + j;
+    if (on && k < p.K) {
+      const int64_t e = static_cast<int64_t>(t) * p.K + k;
+      const int32_t ix = P.perm[e];
+      if (ix >= 0 && static_cast<int64_t>(ix) < P.rows) {
+        idx[j] = ix;
+        sc[j] = load_scale(P.scale, e, p.scale_dtype);
+      }
+    }
   }
-  for (int r = tid; r < p.R; r += nthreads)
-    if (!((p.shared_mask >> r) & 1u)) sh_off[r] = -1;
 }
 
-template <typename A, int RMAX>
-__global__ void __launch_bounds__(1024, 1) cluster_finalize_kernel(const __grid_constant__ KParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+// All KC rows in flight together, then the FMA chain over them in route order.
+template <typename A, int KC>
+__device__ __forceinline__ void gather_chain(const KPartial& P, int H, int vec, const int idx[KC],
+                                             const float sc[KC], float acc[8]) {
+  uint4 d[KC];
+#pragma unroll
+  for (int j = 0; j < KC; ++j)
+    if (idx[j] >= 0) d[j] = ldg16(P.gemm2 + (static_cast<int64_t>(idx[j]) * H + vec * 8) * 2);
+#pragma unroll
+  for (int j = 0; j < KC; ++j) {
+    if (idx[j] >= 0) {
+      float x[8];
+      unpack8<A>(d[j], x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(sc[j], x[i], acc[i]);
+    }
+  }
+}
+
+// Resident CTAs the compiler must allow for (it sets the register budget): two 512-thread CTAs per SM
+// for the 8-routes-in-flight form.
+#ifndef MFR_CLUSTER_MIN_BLOCKS
+#define MFR_CLUSTER_MIN_BLOCKS 2
+#endif
+
+template <typename A, int KC>
+__global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_BLOCKS : 1) cluster_finalize_kernel(const __grid_constant__ KParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
+  const int SV = p.slice_vec;
   const uint32_t C = cluster_nctarank();
   const uint32_t crank = cluster_ctarank();
   const int t = static_cast<int>(blockIdx.x / C);
   const int H = p.H;
-  const int nvec_total = H >> 3;
-  const int v0 = static_cast<int>(crank) * p.slice_vec;
-  const int nv = max(0, min(nvec_total - v0, p.slice_vec));  // 16-byte vectors of this CTA's slice
-  const int stride = p.slice_vec * 16;                       // bytes per staged row
-  const int nslots = p.nslots;
+  const int r = tid / SV;                       // partial of this thread's group
+  const int v = tid - r * SV;
+  const int vec = static_cast<int>(crank) * SV + v;  // 16-byte vector of the hidden row
+  const bool in_group = r < p.R;
+  const bool active = in_group && vec < (H >> 3);
+  uint4* xch = reinterpret_cast<uint4*>(smem);                // [R][SV] shared rows, then partial rows
+  uint4* res_s = xch + p.R * SV;                              // [SV] residual slice
+  uint4* gam_s = res_s + SV;                                  // [SV] gamma slice
+  float* red = reinterpret_cast<float*>(smem + p.off_red);    // [32] warp sums, [32] CTA sum, [33] total
+  const KPartial& P = p.part[in_group ? r : 0];
+  const bool has_shared = in_group && ((p.shared_mask >> r) & 1u);
+  const bool lead = (r == 0) && active;         // group 0 finishes the token
 
-  uint8_t* stage = smem;  // [nslots][slice] act
-  uint8_t* zero_row = smem + p.off_zero;
-  const uint8_t** slot_src = reinterpret_cast<const uint8_t**>(smem + p.off_src);
-  int2* meta = reinterpret_cast<int2*>(smem + p.off_meta);
-  int* sh_off = reinterpret_cast<int*>(smem + p.off_shoff);
-  float* red = reinterpret_cast<float*>(smem + p.off_red);  // [32] warp sums, [32] CTA sum, [33] total
-
-  for (int i = tid; i < p.slice_vec; i += nthreads) reinterpret_cast<uint4*>(zero_row)[i] = make_uint4(0, 0, 0, 0);
+  int idx[KC];
+  float sc[KC];
   if (p.pdl) pdl_launch_dependents();
-  if (p.routing_early) load_slots(p, t, stride, slot_src, meta, sh_off, tid, nthreads);
+  if (p.routing_early) load_routes<KC>(p, P, t, 0, active, idx, sc);
   if (p.pdl) pdl_wait();
-  if (!p.routing_early) load_slots(p, t, stride, slot_src, meta, sh_off, tid, nthreads);
-  __syncthreads();
+  if (!p.routing_early) load_routes<KC>(p, P, t, 0, active, idx, sc);
 
-  // Gather: every valid (slot, 16-byte vector) pair of this slice, all in flight together.
-  const int total = nslots * nv;
-  const uint32_t stage_addr = smem_addr(stage);
-  for (int i = tid; i < total; i += nthreads) {
-    const int s = i / nv;
-    const int v = i - s * nv;
-    const uint8_t* src = slot_src[s];
-    if (src != nullptr)
-      cp_async16(stage_addr + static_cast<uint32_t>(s) * stride + v * 16, src + static_cast<int64_t>(v0 + v) * 16);
+  // Rows that do not depend on the routing go out first, straight into shared memory (each thread
+  // later reads only what it copied itself, after waiting for its own copies).
+  if (has_shared && active)
+    cp_async16(smem_addr(&xch[r * SV + v]), P.shared + (static_cast<int64_t>(t) * H + vec * 8) * 2);
+  if (lead) {
+    cp_async16(smem_addr(&res_s[v]), p.residual + (static_cast<int64_t>(t) * H + vec * 8) * 2);
+    cp_async16(smem_addr(&gam_s[v]), p.gamma + static_cast<int64_t>(vec) * 16);
   }
   cp_async_commit();
 
-  // This thread's 4 elements; residual and gamma load while the gather is in flight.
-  const int el = tid * 4;
-  const bool active = el < nv * 8;
-  const int h = v0 * 8 + el;
-  uint2 res_raw = make_uint2(0, 0), gam_raw = make_uint2(0, 0);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
   if (active) {
-    res_raw = ldg8(p.residual + (static_cast<int64_t>(t) * H + h) * 2);
-    gam_raw = ldg8(p.gamma + static_cast<int64_t>(h) * 2);
+    gather_chain<A, KC>(P, H, vec, idx, sc, acc);
+    for (int k0 = KC; k0 < p.K; k0 += KC) {
+      load_routes<KC>(p, P, t, k0, true, idx, sc);
+      gather_chain<A, KC>(P, H, vec, idx, sc, acc);
+    }
+    // times the routed scaling factor, plus the shared row, rounded once (the partial row p_r)
+    cp_async_wait_all();
+    float shv[8];
+    unpack8<A>(xch[r * SV + v], shv);
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a[i] = __fmul_rn(acc[i], p.rsf);
+      if (has_shared) a[i] = __fadd_rn(a[i], shv[i]);
+    }
+    xch[r * SV + v] = make_uint4(Act<A>::pack(a[0], a[1]), Act<A>::pack(a[2], a[3]), Act<A>::pack(a[4], a[5]),
+                                 Act<A>::pack(a[6], a[7]));
   }
   cp_async_wait_all();
   __syncthreads();
 
-  float S[4] = {0.f, 0.f, 0.f, 0.f}, x[4] = {0.f, 0.f, 0.f, 0.f};
+  // Group 0: rank sum in order 0..R-1, residual add, sum of squares.
+  float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float ss = 0.0f;
-  if (active) {
-    finalize4<A, RMAX>(meta, sh_off, stage, zero_row, el * 2, p.R, p.K, p.rsf, S);
-    const uint2 ro = residual_step<A>(S, res_raw, x, ss);
-    if (p.residual_out != nullptr) stg8(p.residual_out + (static_cast<int64_t>(t) * H + h) * 2, ro);
+  if (lead) {
+    float S[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int rr = 0; rr < p.R; ++rr) {
+      float pr[8];
+      unpack8<A>(xch[rr * SV + v], pr);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) S[i] = __fadd_rn(S[i], pr[i]);
+    }
+    float res[8];
+    unpack8<A>(res_s[v], res);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[i] = Act<A>::round(__fadd_rn(Act<A>::round(S[i]), res[i]));
+      ss = __fmaf_rn(x[i], x[i], ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
+    }
+    if (p.residual_out != nullptr)
+      *reinterpret_cast<uint4*>(p.residual_out + (static_cast<int64_t>(t) * H + vec * 8) * 2) =
+          make_uint4(Act<A>::pack(x[0], x[1]), Act<A>::pack(x[2], x[3]), Act<A>::pack(x[4], x[5]),
+                     Act<A>::pack(x[6], x[7]));
   }
 
   // Sum of squares: warp shuffle, warps in order, then the cluster's CTAs in rank order.
@@ -127,14 +184,18 @@ __global__ void __launch_bounds__(1024, 1) cluster_finalize_kernel(const __grid_
   }
   __syncthreads();
   const float rstd = rms_rstd(red[33], H, p.eps);
-  const float qscale = (p.quant != MFR_QUANT_NONE) ? *p.quant_scale : 1.0f;
-  epilogue4<A>(p, t, h, active, x, gam_raw, rstd, qscale);
+  if (tid < ((SV + 31) & ~31)) {  // the warps that hold group 0 (whole warps, for the NVFP4 shuffles)
+    const float qscale = (p.quant != MFR_QUANT_NONE) ? *p.quant_scale : 1.0f;
+    float g[8];
+    unpack8<A>(lead ? gam_s[v] : make_uint4(0, 0, 0, 0), g);
+    epilogue<A, 8>(p, t, vec * 8, lead, x, g, rstd, qscale);
+  }
   if (C > 1) cluster_wait_acquire();  // no CTA leaves while a peer may still read its shared memory
 }
 
-template <typename A, int RMAX>
+template <typename A, int KC>
 static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  auto kern = cluster_finalize_kernel<A, RMAX>;
+  auto kern = cluster_finalize_kernel<A, KC>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -167,9 +228,9 @@ static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStr
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <typename A, int RMAX>
+template <typename A, int KC>
 static int max_active_clusters(const LaunchGeom& g) {
-  auto kern = cluster_finalize_kernel<A, RMAX>;
+  auto kern = cluster_finalize_kernel<A, KC>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaLaunchConfig_t cfg = {};
@@ -191,22 +252,17 @@ static int max_active_clusters(const LaunchGeom& g) {
   return n;
 }
 
-template <typename A>
-static cudaError_t launch_cluster_r(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  if (p.R <= 1) return launch_cluster<A, 1>(p, g, stream);
-  if (p.R <= 2) return launch_cluster<A, 2>(p, g, stream);
-  if (p.R <= 4) return launch_cluster<A, 4>(p, g, stream);
-  return launch_cluster<A, 8>(p, g, stream);
-}
-
+// Routes in flight per thread: 8 covers top-k <= 8 in one round; larger top-k go 16 at a time.
 cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  return act_dtype == MFR_BF16 ? launch_cluster_r<__nv_bfloat16>(p, g, stream) : launch_cluster_r<__half>(p, g, stream);
+  if (act_dtype == MFR_BF16)
+    return p.K <= 8 ? launch_cluster<__nv_bfloat16, 8>(p, g, stream) : launch_cluster<__nv_bfloat16, 16>(p, g, stream);
+  return p.K <= 8 ? launch_cluster<__half, 8>(p, g, stream) : launch_cluster<__half, 16>(p, g, stream);
 }
 
-// Occupancy of the cluster kernel; the R bound does not change its resources materially, so the
-// widest instantiation answers for all.
-int cluster_kernel_max_active_clusters(int act_dtype, const LaunchGeom& g) {
-  return act_dtype == MFR_BF16 ? max_active_clusters<__nv_bfloat16, 8>(g) : max_active_clusters<__half, 8>(g);
+int cluster_kernel_max_active_clusters(int act_dtype, int K, const LaunchGeom& g) {
+  if (act_dtype == MFR_BF16)
+    return K <= 8 ? max_active_clusters<__nv_bfloat16, 8>(g) : max_active_clusters<__nv_bfloat16, 16>(g);
+  return K <= 8 ? max_active_clusters<__half, 8>(g) : max_active_clusters<__half, 16>(g);
 }
 
 }  // namespace mfr

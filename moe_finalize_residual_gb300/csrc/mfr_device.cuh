@@ -1,7 +1,7 @@
 // Device-side pieces shared by the two finalize kernels: launch parameters, inline-PTX wrappers
 // (cp.async, bulk copies, mbarriers, cluster barriers and DSMEM, programmatic dependent launch),
-// activation-type traits, the per-slot routing metadata and the fused epilogue (RMSNorm output and
-// FP8 / NVFP4 quantisation).
+// activation-type traits, the residual step and the fused epilogue (RMSNorm output and FP8 / NVFP4
+// quantisation).
 //
 // Arithmetic follows the fused MoE finalize of flashinfer PR #6631 "perf(comm): gather MoE-finalize
 // routes together and accumulate in FP32" (Description) and TensorRT-LLM PR #16778 (Fix): FP32
@@ -55,14 +55,14 @@ struct KParams {
   float rsf, eps;
   // cluster kernel
   int32_t slice_vec;      // 16-byte vectors of hidden per CTA (the last CTA may hold fewer)
-  int32_t off_zero, off_src, off_meta, off_shoff, off_red;
+  int32_t off_red;
   // stream kernel
-  int32_t chunk;          // hidden elements per pipeline stage
-  int32_t stages;         // pipeline depth
-  int32_t rdepth;         // routing ring depth (tokens)
-  int32_t stage_bytes;    // bytes of one stage: (nslots + 1 residual) * chunk * 2
-  int32_t ring_bytes;     // bytes of one routing ring entry
-  int32_t off_bar, off_stage, off_ring, off_zero_s, off_gamma, off_stash, off_sred;
+  int32_t chunk;          // hidden elements per pass
+  int32_t stages;         // row buffers in the ring
+  int32_t rdepth;         // row-list ring depth (tokens)
+  int32_t stage_bytes;    // bytes of one row buffer
+  int32_t ring_bytes;     // bytes of one row-list entry
+  int32_t off_bar, off_stage, off_ring, off_gamma, off_stash, off_sred;
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -86,6 +86,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are still in flight (groups retire in order).
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -152,11 +157,6 @@ __device__ __forceinline__ float dsmem_load_f32(const float* local, uint32_t ran
   return v;
 }
 
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ uint2 ldg8(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
 __device__ __forceinline__ void stg8(uint8_t* p, uint2 v) { *reinterpret_cast<uint2*>(p) = v; }
 
 // Deterministic butterfly sum over the 32 lanes of a warp.
@@ -206,103 +206,19 @@ __device__ __forceinline__ void unpack4(uint2 raw, float v[4]) {
   v[3] = b.y;
 }
 
+template <typename A>
+__device__ __forceinline__ void unpack8(uint4 raw, float v[8]) {
+  unpack4<A>(make_uint2(raw.x, raw.y), v);
+  unpack4<A>(make_uint2(raw.z, raw.w), v + 4);
+}
+
+__device__ __forceinline__ uint4 ldg16(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
 __device__ __forceinline__ float load_scale(const void* base, int64_t i, int dtype) {
   if (base == nullptr) return 1.0f;  // absent expert scales read as 1.0
   if (dtype == MFR_FP32) return static_cast<const float*>(base)[i];
   const uint16_t b = static_cast<const uint16_t*>(base)[i];
   return dtype == MFR_BF16 ? __uint_as_float(static_cast<uint32_t>(b) << 16) : __half2float(__ushort_as_half(b));
-}
-
-// ------------------------------------------------------------------------------------------------
-// Routing metadata.  Every row a token may read is a "slot": routes are slots r*K + k, the shared
-// rows of the partials that have one follow as slots R*K + 0, 1, ...  A kernel stages slot s at byte
-// offset s * stride of its stage and describes the token by a table:
-//   meta[r*K + k] = {byte offset of the route's row in the stage, or -1 if the route is skipped;
-//                    bits of its FP32 scale, or of -0.0f if skipped}
-//   sh_off[r]     = byte offset of partial r's shared row, or -1.
-// A skipped route reads a row of zeros with scale -0.0: fma(-0.0, +0.0, acc) == acc for every acc
-// (including -0, infinities and NaN), so skipping costs no branch and changes no bit.
-// ------------------------------------------------------------------------------------------------
-
-__device__ __forceinline__ int shared_slot(const KParams& p, int r) {
-  return p.R * p.K + __popc(p.shared_mask & ((1u << r) - 1u));
-}
-
-struct SlotSource {
-  const uint8_t* src;  // row start in global memory (hidden index 0); nullptr if skipped
-  float scale;
-  int r, k;            // partial and route (k == -1 for a shared row)
-};
-
-// flashinfer PR #6631, Test changes: routes set to -1 contribute nothing; one bound check per route.
-__device__ __forceinline__ SlotSource slot_source(const KParams& p, int s, int t) {
-  SlotSource o;
-  if (s < p.R * p.K) {
-    o.r = s / p.K;
-    o.k = s - o.r * p.K;
-    const KPartial& P = p.part[o.r];
-    const int64_t e = static_cast<int64_t>(t) * p.K + o.k;
-    const int32_t idx = P.perm[e];
-    const bool valid = idx >= 0 && static_cast<int64_t>(idx) < P.rows;
-    o.src = valid ? P.gemm2 + static_cast<int64_t>(idx) * p.H * 2 : nullptr;
-    o.scale = valid ? load_scale(P.scale, e, p.scale_dtype) : -0.0f;
-  } else {
-    int j = s - p.R * p.K;  // j-th partial with a shared row
-    uint32_t m = p.shared_mask;
-    for (; j > 0; --j) m &= m - 1u;
-    o.r = __ffs(m) - 1;
-    o.k = -1;
-    o.src = p.part[o.r].shared + static_cast<int64_t>(t) * p.H * 2;
-    o.scale = 1.0f;
-  }
-  return o;
-}
-
-// Finalize 4 consecutive elements (byte column `col` of every staged row): for each partial the FP32
-// fused multiply-add chain over its routes in order k = 0..K-1 starting from +0, times the routed
-// scaling factor, plus the shared row, rounded once to act; the rounded partials are added to S in
-// rank order 0..R-1 (flashinfer PR #6631, Description; TensorRT-LLM PR #16778, Fix; flashinfer PR
-// #3385, fixed rank order).  The R chains are independent until the rank sum, so they advance
-// together, route by route, which gives each thread 4*R independent FMA chains.
-template <typename A, int RMAX>
-__device__ __forceinline__ void finalize4(const int2* __restrict__ meta, const int* __restrict__ sh_off,
-                                          const uint8_t* stage, const uint8_t* zero_row, int col, int R, int K,
-                                          float rsf, float S[4]) {
-  float acc[RMAX][4];
-#pragma unroll
-  for (int r = 0; r < RMAX; ++r) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[r][i] = 0.0f;
-  }
-#pragma unroll 2
-  for (int k = 0; k < K; ++k) {
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-      if (r < R) {
-        const int2 m = meta[r * K + k];
-        const uint8_t* row = (m.x >= 0) ? stage + m.x : zero_row;
-        float v[4];
-        unpack4<A>(*reinterpret_cast<const uint2*>(row + col), v);
-        const float sc = __int_as_float(m.y);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[r][i] = __fmaf_rn(sc, v[i], acc[r][i]);
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < RMAX; ++r) {
-    if (r < R) {
-      const int so = sh_off[r];
-      float sh[4] = {0.f, 0.f, 0.f, 0.f};
-      if (so >= 0) unpack4<A>(*reinterpret_cast<const uint2*>(stage + so + col), sh);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float a = __fmul_rn(acc[r][i], rsf);
-        if (so >= 0) a = __fadd_rn(a, sh[i]);
-        S[i] = __fadd_rn(S[i], Act<A>::round(a));  // p_r rounded once, summed in FP32 in rank order
-      }
-    }
-  }
 }
 
 // residual_out = round(round(S) + residual); returns the 4 values and adds their squares to ss.
@@ -334,50 +250,73 @@ __device__ __forceinline__ int64_t sf_offset(int64_t m, int64_t k, int H, int la
   return ((m >> 7) * col_tiles + (k >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (k & 3);
 }
 
-// The epilogue for 4 consecutive hidden elements h..h+3 of token t held by one thread: norm_out
-// = round((x * rstd) * gamma), then optional FP8 / NVFP4 quantisation of the rounded values.
-// All 32 lanes of the warp must call it together (NVFP4 blocks span 4 adjacent lanes); lanes with
-// active == false contribute nothing and write nothing.
-template <typename A>
-__device__ __forceinline__ void epilogue4(const KParams& p, int64_t t, int h, bool active, const float x[4],
-                                          uint2 gamma_raw, float rstd, float qscale) {
-  float g[4], y[4];
-  unpack4<A>(gamma_raw, g);
+// The epilogue for N (4 or 8) consecutive hidden elements h..h+N-1 of token t held by one thread:
+// norm_out = round((x * rstd) * gamma), then optional FP8 / NVFP4 quantisation of the rounded values.
+// All 32 lanes of the warp must call it together (an NVFP4 block spans 16/N adjacent lanes); lanes
+// with active == false contribute nothing and write nothing.
+template <typename A, int N>
+__device__ __forceinline__ void epilogue(const KParams& p, int64_t t, int h, bool active, const float x[N],
+                                         const float g[N], float rstd, float qscale) {
+  static_assert(N == 4 || N == 8, "4 or 8 elements per thread");
+  float y[N];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) y[i] = Act<A>::round(__fmul_rn(__fmul_rn(x[i], rstd), g[i]));
+  for (int i = 0; i < N; ++i) y[i] = Act<A>::round(__fmul_rn(__fmul_rn(x[i], rstd), g[i]));
   const int64_t e = t * p.H + h;
-  if (active && p.norm_out != nullptr)
-    stg8(p.norm_out + e * 2, make_uint2(Act<A>::pack(y[0], y[1]), Act<A>::pack(y[2], y[3])));
+  if (active && p.norm_out != nullptr) {
+    uint32_t w[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) w[i] = Act<A>::pack(y[2 * i], y[2 * i + 1]);
+    if constexpr (N == 8)
+      *reinterpret_cast<uint4*>(p.norm_out + e * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+    else
+      *reinterpret_cast<uint2*>(p.norm_out + e * 2) = make_uint2(w[0], w[1]);
+  }
   if (p.quant == MFR_QUANT_FP8_E4M3) {
     if (active) {
-      uint32_t q = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        q |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fmul_rn(y[i], qscale), __NV_SATFINITE, __NV_E4M3))
-             << (8 * i);
-      *reinterpret_cast<uint32_t*>(p.quant_out + e) = q;
+      for (int j = 0; j < N / 4; ++j) {
+        uint32_t q = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          q |= static_cast<uint32_t>(
+                   __nv_cvt_float_to_fp8(__fmul_rn(y[4 * j + i], qscale), __NV_SATFINITE, __NV_E4M3))
+               << (8 * i);
+        *reinterpret_cast<uint32_t*>(p.quant_out + e + 4 * j) = q;
+      }
     }
   } else if (p.quant == MFR_QUANT_NVFP4) {
     float amax = 0.0f;
     if (active) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(y[i]));
+      for (int i = 0; i < N; ++i) amax = fmaxf(amax, fabsf(y[i]));
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+#pragma unroll
+    for (int o = 1; o < 16 / N; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const __nv_fp8_storage_t sf =
         __nv_cvt_float_to_fp8(__fmul_rn(__fdiv_rn(amax, 6.0f), qscale), __NV_SATFINITE, __NV_E4M3);
     const float sf_val = __half2float(__half(__nv_cvt_fp8_to_halfraw(sf, __NV_E4M3)));
     const float es = (sf_val == 0.0f) ? 0.0f : __fdiv_rn(qscale, sf_val);
     if (active) {
-      const uint32_t c01 = __nv_cvt_float2_to_fp4x2(make_float2(__fmul_rn(y[0], es), __fmul_rn(y[1], es)),
-                                                    __NV_E2M1, cudaRoundNearest);
-      const uint32_t c23 = __nv_cvt_float2_to_fp4x2(make_float2(__fmul_rn(y[2], es), __fmul_rn(y[3], es)),
-                                                    __NV_E2M1, cudaRoundNearest);
-      *reinterpret_cast<uint16_t*>(p.quant_out + e / 2) = static_cast<uint16_t>(c01 | (c23 << 8));
+#pragma unroll
+      for (int j = 0; j < N / 4; ++j) {
+        const uint32_t c01 = __nv_cvt_float2_to_fp4x2(
+            make_float2(__fmul_rn(y[4 * j], es), __fmul_rn(y[4 * j + 1], es)), __NV_E2M1, cudaRoundNearest);
+        const uint32_t c23 = __nv_cvt_float2_to_fp4x2(
+            make_float2(__fmul_rn(y[4 * j + 2], es), __fmul_rn(y[4 * j + 3], es)), __NV_E2M1, cudaRoundNearest);
+        *reinterpret_cast<uint16_t*>(p.quant_out + e / 2 + 2 * j) = static_cast<uint16_t>(c01 | (c23 << 8));
+      }
       if ((h & 15) == 0) p.sf_out[sf_offset(t, h >> 4, p.H, p.sf_layout)] = sf;
     }
   }
+}
+
+// The 4-element form used by the stream kernel: gamma arrives as 4 packed act values.
+template <typename A>
+__device__ __forceinline__ void epilogue4(const KParams& p, int64_t t, int h, bool active, const float x[4],
+                                          uint2 gamma_raw, float rstd, float qscale) {
+  float g[4];
+  unpack4<A>(gamma_raw, g);
+  epilogue<A, 4>(p, t, h, active, x, g, rstd, qscale);
 }
 
 }  // namespace mfr
