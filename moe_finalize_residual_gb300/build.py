@@ -29,7 +29,7 @@ def nvcc() -> str:
 
 def _flags(ptxas_verbose: bool):
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
-    f += os.environ.get("MFR_NVCC_FLAGS", "").split()  # e.g. -DMFR_STREAM_CONSUMER_WARPS=8
+    f += os.environ.get("MFR_NVCC_FLAGS", "").split()  # e.g. -DMFR_STREAM_COMPUTE_WARPS=24
     if ptxas_verbose:
         f += ["-Xptxas", "-v"]
     return f

@@ -39,7 +39,7 @@ struct DeviceInfo {
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
 std::map<std::tuple<int, int, int, int, int>, int> g_cluster_ok;  // (dev, act, C, block, smem) -> clusters
-std::map<std::tuple<int, int, int, int>, int> g_stream_bps;       // (dev, act, block, smem) -> blocks/SM
+std::map<std::tuple<int, int, int, int, int>, int> g_stream_bps;  // (dev, act, groups, block, smem) -> blocks/SM
 
 int device_info(DeviceInfo* out, int* dev_out) {
   int dev = 0;
@@ -164,13 +164,10 @@ int pow2_ceil(int x) {
 // Token count up to which the cluster kernel is chosen automatically, and the stream kernel's shape
 // (probe builds may override them).
 #ifndef MFR_CLUSTER_MAX_TOKENS
-#define MFR_CLUSTER_MAX_TOKENS 256
+#define MFR_CLUSTER_MAX_TOKENS 96
 #endif
 #ifndef MFR_CLUSTER_BLOCK
 #define MFR_CLUSTER_BLOCK 512
-#endif
-#ifndef MFR_STREAM_CONSUMER_WARPS
-#define MFR_STREAM_CONSUMER_WARPS 16
 #endif
 constexpr int kClusterMaxTokens = MFR_CLUSTER_MAX_TOKENS;
 constexpr int kMaxCluster = 16;
@@ -220,53 +217,66 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
   return false;
 }
 
-// Stream kernel: persistent CTAs (one per SM), each compute thread copying its own 16-byte columns
-// of the rows ahead into a ring of kStreamSlots row slots.  A hidden pass is the widest multiple of
-// 8 * compute-threads elements (at most kStreamColumns per thread) for which the ring, gamma and the
-// kept residual row fit in shared memory.
+// Stream kernel: persistent CTAs (one per SM) of a routing warp and kStreamGroups groups of compute
+// warps, each group streaming its own tokens.  A compute thread copies its own 16-byte columns of the
+// rows ahead into its group's ring of kStreamSlots row slots; a hidden pass covers 8 elements x
+// kStreamColumns x the group's threads.
 bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
-  const int ncw = MFR_STREAM_CONSUMER_WARPS;
-  const int block = 32 * (1 + ncw);
-  const int step = 8 * 32 * ncw;
-  const int ring_bytes = align_up(16 + p->nslots * 16, 16);
-  const int bar_bytes = 8 * (2 * kStreamLists + 2) + 8;
+  const int block = 32 * (1 + kStreamGroups * kStreamGroupWarps);
+  const int ring_bytes = align_up(16 + (p->nslots + 1) * 16, 16);  // the count, then the entries and the residual row
+  const int bar_bytes = 8 * (2 * kStreamLists + 2 * kStreamGroups) + 8;
   const int off_stage = align_up(bar_bytes, 128);
-  for (int W = step * kStreamColumns; W >= step; W -= step) {
-    const int slot_bytes = std::min(W, a->H) * 2;
-    const int off_ring = off_stage + kStreamSlots * slot_bytes;
-    const int off_gamma = align_up(off_ring + kStreamLists * ring_bytes, 16);
-    const int off_stash = off_gamma + align_up(a->H * 2, 16);
-    const int off_sred = off_stash + align_up(a->H * 2, 16);
-    const int smem = align_up(off_sred + 2 * 32 * 4, 128);
-    if (smem > d.smem_optin) continue;
-    LaunchGeom geo{0, block, 1, smem, d.smem_optin};
-    const auto key = std::make_tuple(dev, a->act_dtype, block, smem);
-    int bps;
-    {
-      std::lock_guard<std::mutex> lock(g_mu);
-      auto it = g_stream_bps.find(key);
-      bps = (it == g_stream_bps.end()) ? -1 : it->second;
+  // With at most one token per CTA (T <= SMs) the groups split each token's hidden dimension (split
+  // mode, pass width H / G); otherwise they split the tokens.  Widest pass first, two groups before
+  // one; narrower passes when shared memory is short.
+  const bool one_token_per_cta = a->T <= d.sms;
+  for (int mode = one_token_per_cta ? 0 : 1; mode < 2; ++mode) {
+  for (int G = kStreamGroups; G >= 1; --G) {
+    if ((kStreamGroups * kStreamGroupWarps) % G != 0 || kStreamLists % G != 0) continue;
+    const bool split = mode == 0;
+    if (split && G < 2) continue;
+    const int step = 8 * 32 * (kStreamGroups * kStreamGroupWarps / G);  // 8 elements x the group's threads
+    const int w_split = align_up(ceil_div(a->H, G), 16);
+    if (split && w_split > step * kStreamColumns) continue;
+    for (int W = split ? w_split : step * kStreamColumns; W >= (split ? w_split : step); W -= step) {
+      const int slot_bytes = std::min(W, a->H) * 2;
+      const int off_ring = off_stage + G * kStreamSlots * slot_bytes;
+      const int off_stash = align_up(off_ring + kStreamLists * ring_bytes, 16);
+      const int off_sred = off_stash + G * align_up(a->H * 2, 16);
+      const int smem = align_up(off_sred + kStreamGroups * 2 * 32 * 4, 128);
+      if (smem > d.smem_optin) continue;
+      LaunchGeom geo{0, block, 1, smem, d.smem_optin};
+      const auto key = std::make_tuple(dev, a->act_dtype, G, block, smem);
+      int bps;
+      {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_stream_bps.find(key);
+        bps = (it == g_stream_bps.end()) ? -1 : it->second;
+      }
+      if (bps < 0) {
+        bps = stream_kernel_blocks_per_sm(a->act_dtype, G, geo);
+        std::lock_guard<std::mutex> lock(g_mu);
+        g_stream_bps[key] = bps;
+      }
+      if (bps < 1) continue;
+      geo.grid = std::min(a->T, d.sms * bps);
+      p->chunk = W;
+      p->stages = kStreamSlots;
+      p->rdepth = kStreamLists;
+      p->stage_bytes = slot_bytes;
+      p->groups = G;
+      p->split = split ? 1 : 0;
+      p->ring_bytes = ring_bytes;
+      p->off_bar = 0;
+      p->off_stage = off_stage;
+      p->off_ring = off_ring;
+      p->off_gamma = 0;
+      p->off_stash = off_stash;
+      p->off_sred = off_sred;
+      *g = geo;
+      return true;
     }
-    if (bps < 0) {
-      bps = stream_kernel_blocks_per_sm(a->act_dtype, geo);
-      std::lock_guard<std::mutex> lock(g_mu);
-      g_stream_bps[key] = bps;
-    }
-    if (bps < 1) continue;
-    geo.grid = std::min(a->T, d.sms * bps);
-    p->chunk = W;
-    p->stages = kStreamSlots;
-    p->rdepth = kStreamLists;
-    p->stage_bytes = slot_bytes;
-    p->ring_bytes = ring_bytes;
-    p->off_bar = 0;
-    p->off_stage = off_stage;
-    p->off_ring = off_ring;
-    p->off_gamma = off_gamma;
-    p->off_stash = off_stash;
-    p->off_sred = off_sred;
-    *g = geo;
-    return true;
+  }
   }
   return false;
 }

@@ -3,19 +3,23 @@
 //
 // Roles:
 //  - routing warp: for each of the CTA's tokens, reads the R*K route indices and scales, checks the
-//    bound of every index, and writes the token's list of rows -- valid routes in order, each
-//    partial's shared row after its routes -- into a ring of lists (kLists tokens deep);
-//  - compute warps: thread j owns 16-byte columns j, j + NCT, j + 2*NCT, ... of every row (8 elements
-//    each; a hidden pass covers 8 * NCT * kQ elements).  Each thread copies ITS OWN columns of the
-//    rows ahead with cp.async (16 bytes, through L2) into a ring of NB row slots, one commit group per
-//    row, up to NB-1 rows ahead and across token boundaries, and later reads only what it copied: the
-//    data needs no barrier, only cp.async.wait_group, which retires groups in issue order.  Every
-//    compute thread issues copies, so the whole CTA keeps rows in flight.  For each row in list order
-//    a thread applies the partial's FP32 fused multiply-add in route order; when the list moves to the
-//    next partial it finishes the previous one (times the routed scaling factor, plus the shared row,
-//    rounded once) into the FP32 rank sum; the residual row closes a pass (residual_out, kept in shared
-//    memory, and the sum of squares).  After a token's last pass the compute warps reduce the sum of
-//    squares and write norm_out and the quantised output from the kept values and gamma.
+//    bound of every index, and writes the token's list of rows into a ring of lists (kLists tokens
+//    deep): valid routes in order, each partial's shared row after its routes, the residual row last;
+//    each entry carries its partial and whether it is the partial's last row;
+//  - compute warps, in G groups that run separate token streams (or, with at most one token per CTA,
+//    split each token's hidden dimension between them): thread j of a group owns 16-byte columns
+//    j, j + NCT, j + 2*NCT, ... of every row (8 elements each; a hidden pass covers 8 * NCT * kQ
+//    elements).  Each thread copies ITS OWN columns of the rows ahead with cp.async (16 bytes, through
+//    L2) into its group's ring of NB row slots, one commit group per row, up to NB-1 rows ahead and
+//    across token boundaries, and later reads only what it copied: the data needs no barrier, only
+//    cp.async.wait_group, which retires groups in issue order.  Per row a thread applies the partial's
+//    FP32 fused multiply-add (or the shared-row step); after a partial's last row it rounds the
+//    partial once into the FP32 rank sum; the residual row closes a pass (residual_out, kept in shared
+//    memory, and the sum of squares).  After a token's last pass the group reduces the sum of squares
+//    and writes norm_out and the quantised output from the kept values and gamma.
+//
+// The group shape is a compile-time constant, so a thread's column offsets are immediates and the
+// per-row work is the copies, the arithmetic and a few cursor updates.
 //
 // Prior art: flashinfer PR #6546 (large-batch finalizeKernelVecLoad path); flashinfer PR #3385
 // (RMSNorm inputs staged in shared memory).  The arithmetic is that of flashinfer PR #6631,
@@ -39,14 +43,16 @@ constexpr int kRoutingWarp = 0;
 constexpr int kFirstComputeWarp = 1;
 constexpr int kQ = kStreamColumns;    // 16-byte columns per compute thread per pass
 constexpr int kLists = kStreamLists;  // row lists in the ring (tokens)
-constexpr uint32_t kRowShared = 0x100u;
+constexpr uint32_t kTagPartial = 0xffu;
+constexpr uint32_t kTagShared = 0x100u;    // the partial's shared row
+constexpr uint32_t kTagResidual = 0x200u;  // the residual row (closes a pass)
+constexpr uint32_t kTagLast = 0x400u;      // the partial's last row: round it into the rank sum after
 
-// One listed row of a token: where it starts, its scale, its partial (and whether it is the
-// partial's shared row).
+// One listed row of a token: where it starts, its scale and its tag.
 struct RowEntry {
   const uint8_t* src;
   float scale;
-  uint32_t tag;  // partial index | kRowShared
+  uint32_t tag;
 };
 
 // Bounded wait.  Returns false if the CTA is aborting or the limit ran out (then it starts the abort).
@@ -71,15 +77,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag));
 }
 
-// Finish partial rows into the rank sum: acc (times the factor unless the shared row already applied
-// it), rounded once, added to S in FP32; acc restarts from +0.
+// Round a finished partial into the rank sum: acc (times the factor unless the partial's shared row
+// already applied it), rounded once, added to S in FP32; acc restarts from +0.  Element pairs use the
+// packed FP32 operations, which round each lane like the scalar ones (the rounding to act between the
+// multiply and the add keeps them from being contracted).
 template <typename A>
-__device__ __forceinline__ void flush_partial(float acc[kQ * 8], float S[kQ * 8], bool shared_done, float rsf) {
+__device__ __forceinline__ void flush_partial(float2 acc[kQ * 4], float2 S[kQ * 4], bool shared_done, float rsf) {
+  const float2 f = make_float2(rsf, rsf);
 #pragma unroll
-  for (int i = 0; i < kQ * 8; ++i) {
-    const float a = shared_done ? acc[i] : __fmul_rn(acc[i], rsf);
-    S[i] = __fadd_rn(S[i], Act<A>::round(a));
-    acc[i] = 0.0f;
+  for (int i = 0; i < kQ * 4; ++i) {
+    const float2 a = shared_done ? acc[i] : __fmul2_rn(acc[i], f);
+    S[i] = __fadd2_rn(S[i], round_pair<A>(a));
+    acc[i] = make_float2(0.0f, 0.0f);
   }
 }
 
@@ -96,8 +105,9 @@ __device__ __forceinline__ void slot_in_list_order(const KParams& p, int s, int&
   if (k >= p.K) k = -1;
 }
 
-// The routing warp's list for token t (valid routes in order, then the partial's shared row), compacted
-// with a warp ballot.  Returns the number of rows.
+// The routing warp's list for token t: valid routes in order and the partial's shared row, compacted
+// with a warp ballot, each partial's last row tagged, then the residual row.  Returns the number of
+// entries (at least 1).
 __device__ __forceinline__ int build_row_list(const KParams& p, int t, RowEntry* list, int lane) {
   int n = 0;
   for (int base = 0; base < p.nslots; base += 32) {
@@ -111,7 +121,7 @@ __device__ __forceinline__ int build_row_list(const KParams& p, int t, RowEntry*
       if (k < 0) {
         row.src = P.shared + static_cast<int64_t>(t) * p.H * 2;
         row.scale = 1.0f;
-        row.tag = static_cast<uint32_t>(r) | kRowShared;
+        row.tag = static_cast<uint32_t>(r) | kTagShared;
         valid = true;
       } else {
         // flashinfer PR #6631, Test changes: -1 routes contribute nothing; one bound check per route.
@@ -129,40 +139,61 @@ __device__ __forceinline__ int build_row_list(const KParams& p, int t, RowEntry*
     if (valid) list[n + __popc(ballot & ((1u << lane) - 1u))] = row;
     n += __popc(ballot);
   }
-  return n;
+  __syncwarp();
+  // An entry is its partial's last row when the next entry belongs to another partial (or there is
+  // none).  All reads of a round happen before its writes.
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const uint32_t tag = (i < n) ? list[i].tag : 0u;
+    const bool last = (i < n) && (i + 1 == n || (list[i + 1].tag & kTagPartial) != (tag & kTagPartial));
+    __syncwarp();
+    if (last) list[i].tag = tag | kTagLast;
+    __syncwarp();
+  }
+  if (lane == 0) {
+    RowEntry res;
+    res.src = p.residual + static_cast<int64_t>(t) * p.H * 2;
+    res.scale = 1.0f;
+    res.tag = kTagResidual;
+    list[n] = res;
+  }
+  return n + 1;
 }
 
-constexpr int kNB = kStreamSlots;     // row slots in the ring
-constexpr int kLook = kNB - 1;        // rows in flight ahead of the one being read
+constexpr int kNB = kStreamSlots;  // row slots in a group's ring
+constexpr int kLook = kNB - 1;     // rows in flight ahead of the one being read
 
-template <typename A>
+// G groups of compute warps; G is a template parameter so that a thread's column offsets are
+// immediates.
+template <typename A, int G>
 __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(const __grid_constant__ KParams p) {
+  constexpr int NCW = kStreamGroups * kStreamGroupWarps / G;  // compute warps per group
+  constexpr int NCT = 32 * NCW;                               // threads per group
+  constexpr int QB = NCT * 16;                                // bytes between a thread's columns
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int ncw = static_cast<int>(blockDim.x >> 5) - kFirstComputeWarp;  // compute warps
-  const int nct = ncw * 32;
   const int H = p.H, W = p.chunk;
   const int npass = (H + W - 1) / W;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   const uint32_t rfull0 = smem_addr(bars);       // kLists: row list written (routing warp)
   const uint32_t rempty0 = rfull0 + 8u * kLists; // kLists: row list released (one arrival per compute warp)
-  const uint32_t cbar0 = rempty0 + 8u * kLists;  // 2: compute warps done with a token (by parity)
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kLists + 2);
-  uint8_t* slots = smem + p.off_stage;           // kNB row slots of p.stage_bytes
+  const uint32_t cbar0 = rempty0 + 8u * kLists;  // 2 per group: its warps done with a token (by parity)
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kLists + 2 * kStreamGroups);
   uint8_t* ring0 = smem + p.off_ring;
-  uint8_t* gamma_s = smem + p.off_gamma;
-  uint8_t* stash = smem + p.off_stash;
-  float* sred = reinterpret_cast<float*>(smem + p.off_sred);  // [2][32]
 
   if (tid == 0) {
     for (int i = 0; i < kLists; ++i) {
       mbar_init(rfull0 + 8u * i, 1);
-      mbar_init(rempty0 + 8u * i, static_cast<uint32_t>(ncw));
+      mbar_init(rempty0 + 8u * i, static_cast<uint32_t>(p.split ? G * NCW : NCW));
     }
-    mbar_init(cbar0, static_cast<uint32_t>(ncw));
-    mbar_init(cbar0 + 8u, static_cast<uint32_t>(ncw));
+    if (p.split) {  // all groups work on every token: one reduction barrier pair for the CTA
+      mbar_init(cbar0, static_cast<uint32_t>(G * NCW));
+      mbar_init(cbar0 + 8u, static_cast<uint32_t>(G * NCW));
+    } else {
+      for (int i = 0; i < 2 * G; ++i) mbar_init(cbar0 + 8u * i, static_cast<uint32_t>(NCW));
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -187,182 +218,201 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
       if (lane == 0) mbar_arrive(rfull0 + 8u * slot);
     }
   } else {
-    const int jt = tid - kFirstComputeWarp * 32;  // compute thread: owns 16-byte columns jt + nct*q
-    const int cw = warp - kFirstComputeWarp;
+    const int jall = tid - kFirstComputeWarp * 32;
+    // Groups split the tokens (group g takes tokens g, g + G, ...; every pass) or, in split mode, each
+    // token's hidden passes (group g takes pass g of every token).
+    const int grp = jall / NCT;
+    const int jt = jall - grp * NCT;  // owns 16-byte columns jt + NCT*q of every row
+    const int cw = (jall >> 5) - grp * NCW;
+    const int tok0 = p.split ? 0 : grp, tstride = p.split ? 1 : G;
+    const int pass_lo = p.split ? grp : 0, pass_hi = p.split ? grp + 1 : npass;
+    const int nred = p.split ? G * NCW : NCW, ridx = p.split ? grp * NCW + cw : cw;  // sum-of-squares slots
     const float qscale = (p.quant != MFR_QUANT_NONE) ? *p.quant_scale : 1.0f;
-
-    // This thread's columns of gamma (they travel with the first row's copies).
-    for (int pass = 0; pass < npass; ++pass) {
+    const uint32_t slot0 =
+        smem_addr(smem + p.off_stage + static_cast<size_t>(grp) * kNB * p.stage_bytes) + jt * 16;
+    const uint32_t slot_end = slot0 + kNB * p.stage_bytes;
+    uint8_t* stash = smem + p.off_stash + (p.split ? 0 : static_cast<size_t>(grp) * ((H * 2 + 15) & ~15));
+    float* sred = reinterpret_cast<float*>(smem + p.off_sred) + (p.split ? 0 : grp * 64);  // [2][32]
+    const uint32_t gcbar = p.split ? cbar0 : cbar0 + 16u * grp;
+    // Columns of this thread that fall inside pass ps (bit q for column q).
+    auto colmask = [&](int ps) -> uint32_t {
+      const int lim = min(W, H - ps * W);
+      uint32_t m = 0;
 #pragma unroll
-      for (int q = 0; q < kQ; ++q) {
-        const int el = 8 * jt + 8 * nct * q, h = pass * W + el;
-        if (el < W && h < H) cp_async16(smem_addr(gamma_s + static_cast<int64_t>(h) * 2), p.gamma + static_cast<int64_t>(h) * 2);
-      }
-    }
+      for (int q = 0; q < kQ; ++q)
+        if ((jt + q * NCT) * 8 < lim) m |= 1u << q;
+      return m;
+    };
 
-    // Issue cursor: token ii (local index), pass ip and row ij (0..n, n = the residual row) of it.
-    int ii = 0, ip = 0, ij = 0, in_n = -1;
+    // Issue cursor: token ii (local index), pass ip and entry ij of its list (in_n entries).
+    int ii = tok0, ip = pass_lo, ij = 0, in_n = -1;
     const RowEntry* ilist = nullptr;
-    uint32_t gi = 0;
+    uint32_t idst = slot0, imask = colmask(pass_lo);
+    int64_t ipoff = static_cast<int64_t>(pass_lo) * W * 2 + jt * 16;  // this thread's first column in a row
+    int issued = 0;  // rows issued (one commit group each)
     // Consume cursor (the same walk).
-    int ci = 0, cp_ = 0, cj = 0, cn = -1;
+    int ci = tok0, cpass = pass_lo, cj = 0, cn = -1;
     const RowEntry* clist = nullptr;
-    uint32_t gc = 0;
+    uint32_t cdst = slot0, cmask = imask;
+    int consumed = 0;
     bool ok = true;
 
-    // Issue this thread's columns of the next row (if there is one it may issue) and commit a group.
+    // Issue this thread's columns of the next row, if there is one it may issue: a list is reused only
+    // after its token is consumed, so the cursor stays fewer than kLists tokens ahead.
     auto issue_one = [&]() {
-      if (ok && ii < ntok && ii < ci + kLists) {  // a list is reused only after its token is consumed
-        if (in_n < 0) {
-          const int slot = ii % kLists;
-          if (warp_wait(rfull0 + 8u * slot, static_cast<uint32_t>(ii / kLists) & 1u, abort_flag)) {
-            const uint8_t* e = ring0 + slot * p.ring_bytes;
-            in_n = *reinterpret_cast<const int*>(e);
-            ilist = reinterpret_cast<const RowEntry*>(e + 16);
-          } else {
-            ok = false;
-          }
+      if (!(ok && ii < ntok && ii < ci + kLists)) return;
+      if (in_n < 0) {
+        const int slot = ii % kLists;
+        if (!warp_wait(rfull0 + 8u * slot, static_cast<uint32_t>(ii / kLists) & 1u, abort_flag)) {
+          ok = false;
+          return;
         }
-        if (ok) {
-          const int t = static_cast<int>(blockIdx.x) + ii * static_cast<int>(gridDim.x);
-          const uint8_t* src = (ij < in_n) ? ilist[ij].src : p.residual + static_cast<int64_t>(t) * H * 2;
-          const int h0 = ip * W;
-          uint8_t* dst = slots + static_cast<size_t>(gi % kNB) * p.stage_bytes;
-#pragma unroll
-          for (int q = 0; q < kQ; ++q) {
-            const int el = 8 * jt + 8 * nct * q;
-            if (el < W && h0 + el < H)
-              cp_async16(smem_addr(dst + el * 2), src + static_cast<int64_t>(h0 + el) * 2);
-          }
-          ++gi;
-          if (++ij > in_n) {
-            ij = 0;
-            if (++ip == npass) {
-              ip = 0;
-              ++ii;
-              in_n = -1;
-            }
-          }
-        }
+        const uint8_t* e = ring0 + slot * p.ring_bytes;
+        in_n = *reinterpret_cast<const int*>(e);
+        ilist = reinterpret_cast<const RowEntry*>(e + 16);
       }
+      const uint8_t* src = ilist[ij].src + ipoff;
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) cp_async16_if(idst + q * QB, src + q * QB, (imask >> q) & 1u);
       cp_async_commit();
+      ++issued;
+      idst += p.stage_bytes;
+      if (idst == slot_end) idst = slot0;
+      if (++ij == in_n) {
+        ij = 0;
+        if (++ip == pass_hi) {
+          ip = pass_lo;
+          ii += tstride;
+          in_n = -1;
+        }
+        ipoff = static_cast<int64_t>(ip) * W * 2 + jt * 16;
+        imask = colmask(ip);
+      }
     };
 
     for (int s = 0; s < kLook; ++s) issue_one();
 
-    float acc[kQ * 8], S[kQ * 8];
+    float2 acc[kQ * 4], S[kQ * 4];
 #pragma unroll
-    for (int i = 0; i < kQ * 8; ++i) acc[i] = S[i] = 0.0f;
+    for (int i = 0; i < kQ * 4; ++i) acc[i] = S[i] = make_float2(0.0f, 0.0f);
     float ss = 0.0f;
-    int cur = -1;
-    bool shared_done = false;
 
     while (ok && ci < ntok) {
       issue_one();
-      cp_async_wait_group<kLook>();  // this thread's columns of row gc have landed
+      // This thread's columns of row `consumed` are in the group issued `issued - consumed - 1` groups
+      // before the newest; with fewer than kLook rows ahead, wait for all of them.
+      if (issued - consumed > kLook) cp_async_wait_group<kLook>();
+      else cp_async_wait_all();
+      if (!ok) break;
       if (cn < 0) {  // the issue cursor already waited for this token's list
         const uint8_t* e = ring0 + (ci % kLists) * p.ring_bytes;
         cn = *reinterpret_cast<const int*>(e);
         clist = reinterpret_cast<const RowEntry*>(e + 16);
       }
-      const int t = static_cast<int>(blockIdx.x) + ci * static_cast<int>(gridDim.x);
-      const int jr = cj;
-      const int h0 = cp_ * W;
-      const uint8_t* row = slots + static_cast<size_t>(gc % kNB) * p.stage_bytes;
-      if (jr < cn) {
-        const RowEntry ent = clist[jr];
-        const int r = static_cast<int>(ent.tag & 0xffu);
-        if (r != cur) {  // the list moved to the next partial: finish the previous one
-          if (cur >= 0) flush_partial<A>(acc, S, shared_done, p.rsf);
-          cur = r;
-          shared_done = false;
-        }
-        const bool is_shared = (ent.tag & kRowShared) != 0;  // the same for the whole CTA
-        if (is_shared) {
-#pragma unroll
-          for (int q = 0; q < kQ; ++q) {
-            const int el = 8 * jt + 8 * nct * q;
-            if (el < W && h0 + el < H) {
-              float v[8];
-              unpack8<A>(*reinterpret_cast<const uint4*>(row + el * 2), v);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) acc[8 * q + c] = __fadd_rn(__fmul_rn(acc[8 * q + c], p.rsf), v[c]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < kQ; ++q) {
-            const int el = 8 * jt + 8 * nct * q;
-            if (el < W && h0 + el < H) {
-              float v[8];
-              unpack8<A>(*reinterpret_cast<const uint4*>(row + el * 2), v);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) acc[8 * q + c] = __fmaf_rn(ent.scale, v[c], acc[8 * q + c]);
-            }
-          }
-        }
-        shared_done = shared_done || is_shared;
-      } else {  // the residual row closes the pass
-        if (cur >= 0) flush_partial<A>(acc, S, shared_done, p.rsf);
-        cur = -1;
-        shared_done = false;
+      // The entry: source (unused here), scale and tag.
+      const uint4 ent = lds16(smem_addr(clist + cj));
+      const float scale = __uint_as_float(ent.z);
+      const uint32_t tag = ent.w;
+      // Columns outside the pass read as zeros and are never stored, so the arithmetic needs no branch.
+      if (!(tag & (kTagShared | kTagResidual))) {  // a routed row: acc += scale * row, fused
+        const float2 sc = make_float2(scale, scale);
 #pragma unroll
         for (int q = 0; q < kQ; ++q) {
-          const int el = 8 * jt + 8 * nct * q;
-          if (el < W && h0 + el < H) {
-            const uint4 res_raw = *reinterpret_cast<const uint4*>(row + el * 2);
-            float x[8];
-            const uint2 lo = residual_step<A>(&S[8 * q], make_uint2(res_raw.x, res_raw.y), x, ss);
-            const uint2 hi = residual_step<A>(&S[8 * q + 4], make_uint2(res_raw.z, res_raw.w), x + 4, ss);
-            const uint4 ro = make_uint4(lo.x, lo.y, hi.x, hi.y);
-            *reinterpret_cast<uint4*>(stash + static_cast<int64_t>(h0 + el) * 2) = ro;
+          float2 v[4];
+          unpack_pairs<A>(lds16_if(cdst + q * QB, (cmask >> q) & 1u), v);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[4 * q + c] = __ffma2_rn(sc, v[c], acc[4 * q + c]);
+        }
+        if (tag & kTagLast) flush_partial<A>(acc, S, false, p.rsf);
+      } else if (tag & kTagShared) {  // acc times the factor, rounded, plus the shared row (last)
+        // Scalar operations here: a packed multiply followed by a packed add of its result may be
+        // contracted into one packed FMA, which rounds once instead of twice.
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          float2 v[4];
+          unpack_pairs<A>(lds16_if(cdst + q * QB, (cmask >> q) & 1u), v);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float2& a = acc[4 * q + c];
+            a = make_float2(__fadd_rn(__fmul_rn(a.x, p.rsf), v[c].x), __fadd_rn(__fmul_rn(a.y, p.rsf), v[c].y));
+          }
+        }
+        flush_partial<A>(acc, S, true, p.rsf);
+      } else {  // the residual row closes the pass: residual_out = round(round(S) + residual)
+        const int t = static_cast<int>(blockIdx.x) + ci * static_cast<int>(gridDim.x);
+        const int64_t hoff = static_cast<int64_t>(cpass) * W + jt * 8;  // element of column 0
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          if (cmask & (1u << q)) {
+            float2 res[4];
+            unpack_pairs<A>(lds16(cdst + q * QB), res);
+            uint32_t w[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float2 x = round_pair<A>(__fadd2_rn(round_pair<A>(S[4 * q + c]), res[c]));
+              ss = __fmaf_rn(x.x, x.x, ss);  // the squares are exact for 16-bit values
+              ss = __fmaf_rn(x.y, x.y, ss);
+              w[c] = Act<A>::pack(x.x, x.y);
+            }
+            const uint4 ro = make_uint4(w[0], w[1], w[2], w[3]);
+            const int64_t h = hoff + q * NCT * 8;
+            *reinterpret_cast<uint4*>(stash + h * 2) = ro;
             if (p.residual_out != nullptr)
-              *reinterpret_cast<uint4*>(p.residual_out + (static_cast<int64_t>(t) * H + h0 + el) * 2) = ro;
+              *reinterpret_cast<uint4*>(p.residual_out + (static_cast<int64_t>(t) * H + h) * 2) = ro;
           }
         }
 #pragma unroll
-        for (int i = 0; i < kQ * 8; ++i) S[i] = 0.0f;
+        for (int i = 0; i < kQ * 4; ++i) S[i] = make_float2(0.0f, 0.0f);
       }
-      ++gc;
-      if (++cj <= cn) continue;
+      ++consumed;
+      cdst += p.stage_bytes;
+      if (cdst == slot_end) cdst = slot0;
+      if (++cj < cn) continue;
       cj = 0;
-      if (++cp_ < npass) continue;
-      cp_ = 0;
+      if (++cpass < pass_hi) {
+        cmask = colmask(cpass);
+        continue;
+      }
+      cpass = pass_lo;
+      cmask = colmask(cpass);
 
-      // Token done: release its list, reduce the sum of squares over the compute warps (in warp order,
-      // double-buffered by token parity; the warps meet on an mbarrier so the wait is bounded), write
-      // norm_out and the quantised output from the kept residual_out and gamma.
+      // Token done: release its list, reduce the sum of squares over the group's warps (all compute
+      // warps in split mode), in warp order, double-buffered by token parity (the warps meet on an
+      // mbarrier so the wait is bounded), and write norm_out and the quantised output from the kept
+      // residual_out and gamma.
       __syncwarp();
       if (lane == 0) mbar_arrive(rempty0 + 8u * (ci % kLists));
       const float wsum = warp_sum(ss);
-      float* rb = sred + (ci & 1) * 32;
+      const int k = ci / tstride;  // the group's k-th token
+      float* rb = sred + (k & 1) * 32;
       if (lane == 0) {
-        rb[cw] = wsum;
-        mbar_arrive(cbar0 + 8u * (ci & 1));
+        rb[ridx] = wsum;
+        mbar_arrive(gcbar + 8u * (k & 1));
       }
-      if (!warp_wait(cbar0 + 8u * (ci & 1), static_cast<uint32_t>(ci >> 1) & 1u, abort_flag)) {
+      if (!warp_wait(gcbar + 8u * (k & 1), static_cast<uint32_t>(k >> 1) & 1u, abort_flag)) {
         ok = false;
         break;
       }
       float tot = 0.0f;
-      for (int w2 = 0; w2 < ncw; ++w2) tot = __fadd_rn(tot, rb[w2]);
+      for (int w2 = 0; w2 < nred; ++w2) tot = __fadd_rn(tot, rb[w2]);
       const float rstd = rms_rstd(tot, H, p.eps);
-      for (int ps = 0; ps < npass; ++ps) {
+      const int t = static_cast<int>(blockIdx.x) + ci * static_cast<int>(gridDim.x);
+      for (int ps = pass_lo; ps < pass_hi; ++ps) {
+        const uint32_t m = colmask(ps);
 #pragma unroll
         for (int q = 0; q < kQ; ++q) {
-          const int el = 8 * jt + 8 * nct * q;
-          const int h = ps * W + el;
-          const bool active = el < W && h < H;
+          const int h = ps * W + (jt + q * NCT) * 8;
+          const bool active = (m >> q) & 1u;
           float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, g[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           if (active) {
             unpack8<A>(*reinterpret_cast<const uint4*>(stash + static_cast<int64_t>(h) * 2), x);
-            unpack8<A>(*reinterpret_cast<const uint4*>(gamma_s + static_cast<int64_t>(h) * 2), g);
+            unpack8<A>(ldg16(p.gamma + static_cast<int64_t>(h) * 2), g);
           }
           epilogue<A, 8>(p, t, h, active, x, g, rstd, qscale);
         }
       }
       ss = 0.0f;
-      ++ci;
+      ci += tstride;
       cn = -1;
     }
     cp_async_wait_all();  // no copy of this thread may land after the CTA exits
@@ -370,9 +420,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
   __syncthreads();
 }
 
-template <typename A>
+template <typename A, int G>
 static cudaError_t launch_stream(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  auto kern = stream_finalize_kernel<A>;
+  auto kern = stream_finalize_kernel<A, G>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -398,13 +448,19 @@ static cudaError_t launch_stream(const KParams& p, const LaunchGeom& g, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  return act_dtype == MFR_BF16 ? launch_stream<__nv_bfloat16>(p, g, stream) : launch_stream<__half>(p, g, stream);
+template <typename A>
+static cudaError_t launch_stream_groups(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
+  return p.groups == 2 ? launch_stream<A, 2>(p, g, stream) : launch_stream<A, 1>(p, g, stream);
 }
 
-template <typename A>
+cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
+  return act_dtype == MFR_BF16 ? launch_stream_groups<__nv_bfloat16>(p, g, stream)
+                               : launch_stream_groups<__half>(p, g, stream);
+}
+
+template <typename A, int G>
 static int blocks_per_sm(const LaunchGeom& g) {
-  auto kern = stream_finalize_kernel<A>;
+  auto kern = stream_finalize_kernel<A, G>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, g.block, g.smem) != cudaSuccess) {
@@ -414,8 +470,10 @@ static int blocks_per_sm(const LaunchGeom& g) {
   return n;
 }
 
-int stream_kernel_blocks_per_sm(int act_dtype, const LaunchGeom& g) {
-  return act_dtype == MFR_BF16 ? blocks_per_sm<__nv_bfloat16>(g) : blocks_per_sm<__half>(g);
+int stream_kernel_blocks_per_sm(int act_dtype, int groups, const LaunchGeom& g) {
+  if (act_dtype == MFR_BF16)
+    return groups == 2 ? blocks_per_sm<__nv_bfloat16, 2>(g) : blocks_per_sm<__nv_bfloat16, 1>(g);
+  return groups == 2 ? blocks_per_sm<__half, 2>(g) : blocks_per_sm<__half, 1>(g);
 }
 
 cudaError_t read_and_reset_timeouts(unsigned int* count) {

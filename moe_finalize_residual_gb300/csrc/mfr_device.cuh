@@ -61,6 +61,8 @@ struct KParams {
   int32_t stages;         // row buffers in the ring
   int32_t rdepth;         // row-list ring depth (tokens)
   int32_t stage_bytes;    // bytes of one row buffer
+  int32_t groups;         // stream kernel: groups of compute warps per CTA
+  int32_t split;          // stream kernel: groups split each token's hidden passes (else the tokens)
   int32_t ring_bytes;     // bytes of one row-list entry
   int32_t off_bar, off_stage, off_ring, off_gamma, off_stash, off_sred;
 };
@@ -83,6 +85,32 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // 16-byte asynchronous global -> shared copy through L2 (bypassing L1).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// The same copy under a predicate (no branch): nothing is copied when `on` is false.
+__device__ __forceinline__ void cp_async16_if(uint32_t dst, const void* src, bool on) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p cp.async.cg.shared.global [%0], [%1], 16;\n}\n" ::"r"(dst),
+      "l"(src), "r"(static_cast<int>(on))
+      : "memory");
+}
+// 16-byte shared-memory load under a predicate (zeros when `on` is false).
+__device__ __forceinline__ uint4 lds16_if(uint32_t addr, bool on) {
+  uint4 v;
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %5, 0;\n mov.b32 %0, 0;\n mov.b32 %1, 0;\n mov.b32 %2, 0;\n"
+      " mov.b32 %3, 0;\n @p ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n}\n"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "r"(addr), "r"(static_cast<int>(on))
+      : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
@@ -206,6 +234,22 @@ __device__ __forceinline__ void unpack4(uint2 raw, float v[4]) {
   v[3] = b.y;
 }
 
+// 8 act values as 4 FP32 pairs, for the packed FP32 operations of sm_100 and later (__ffma2_rn and
+// friends round each lane exactly like the scalar operation).
+template <typename A>
+__device__ __forceinline__ void unpack_pairs(uint4 raw, float2 v[4]) {
+  v[0] = Act<A>::unpack(raw.x);
+  v[1] = Act<A>::unpack(raw.y);
+  v[2] = Act<A>::unpack(raw.z);
+  v[3] = Act<A>::unpack(raw.w);
+}
+
+// Round both lanes to act and back to FP32.
+template <typename A>
+__device__ __forceinline__ float2 round_pair(float2 a) {
+  return Act<A>::unpack(Act<A>::pack(a.x, a.y));
+}
+
 template <typename A>
 __device__ __forceinline__ void unpack8(uint4 raw, float v[8]) {
   unpack4<A>(make_uint2(raw.x, raw.y), v);
@@ -213,6 +257,15 @@ __device__ __forceinline__ void unpack8(uint4 raw, float v[8]) {
 }
 
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// 16-byte load of data read once: through the non-coherent path, without allocating in L1.
+__device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ float load_scale(const void* base, int64_t i, int dtype) {
   if (base == nullptr) return 1.0f;  // absent expert scales read as 1.0

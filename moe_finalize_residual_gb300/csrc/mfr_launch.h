@@ -7,11 +7,29 @@
 
 namespace mfr {
 
-constexpr int kStreamMaxThreads = 544;   // a routing warp + up to 16 compute warps
-constexpr int kClusterMaxThreads = 512;  // R groups of SV threads
-constexpr int kStreamSlots = 12;         // row slots in the stream kernel's shared-memory ring
-constexpr int kStreamLists = 4;          // row lists (tokens) in its routing ring
-constexpr int kStreamColumns = 2;        // 16-byte columns per compute thread per hidden pass
+// Stream kernel shape (probe builds may override the defaults): a routing warp and kStreamGroups
+// groups of compute warps, each group running its own stream of tokens.
+#ifndef MFR_STREAM_GROUPS
+#define MFR_STREAM_GROUPS 2
+#endif
+#ifndef MFR_STREAM_GROUP_WARPS
+#define MFR_STREAM_GROUP_WARPS 7
+#endif
+#ifndef MFR_STREAM_COLUMNS
+#define MFR_STREAM_COLUMNS 4
+#endif
+#ifndef MFR_STREAM_SLOTS
+#define MFR_STREAM_SLOTS 6
+#endif
+constexpr int kStreamGroups = MFR_STREAM_GROUPS;
+constexpr int kStreamGroupWarps = MFR_STREAM_GROUP_WARPS;
+constexpr int kStreamMaxThreads = 32 * (1 + MFR_STREAM_GROUPS * MFR_STREAM_GROUP_WARPS);
+constexpr int kStreamSlots = MFR_STREAM_SLOTS;      // row slots per group in shared memory
+constexpr int kStreamLists = 4;                     // row lists (tokens) in the routing ring
+constexpr int kStreamColumns = MFR_STREAM_COLUMNS;  // 16-byte columns per compute thread per hidden pass
+static_assert(kStreamLists % kStreamGroups == 0, "a list slot must return to the group that used it");
+static_assert(kStreamGroups == 1 || kStreamGroups == 2, "the stream kernel is built for one or two groups");
+constexpr int kClusterMaxThreads = 512;             // R groups of SV threads
 
 struct LaunchGeom {
   int grid;
@@ -24,7 +42,7 @@ struct LaunchGeom {
 cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
 int cluster_kernel_max_active_clusters(int act_dtype, int K, const LaunchGeom& g);
 cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
-int stream_kernel_blocks_per_sm(int act_dtype, const LaunchGeom& g);
+int stream_kernel_blocks_per_sm(int act_dtype, int groups, const LaunchGeom& g);
 cudaError_t read_and_reset_timeouts(unsigned int* count);
 
 }  // namespace mfr

@@ -174,3 +174,19 @@ def check_quant(res: Result, act, quant: str, qscale: float, sf_layout: str, T: 
             got_b = got_q.reshape(T, H // 16, 8)
             ful_b = q_full.reshape(T, H // 16, 8)
             assert np.array_equal(got_b[blk_same], ful_b[blk_same])
+
+
+def contraction_case(act, T: int = 64, H: int = 1024, R: int = 2) -> synth.Case:
+    """A case that tells "acc times the factor, rounded, then plus the shared row" from one fused
+    multiply-add: one route per token with scale 1 (so acc is the gathered row itself), a factor with a
+    full 24-bit significand (so the FP32 product is inexact), shared rows equal to minus the product
+    rounded to act (so the add cancels the leading bits and exposes the product's rounding), and a zero
+    residual (so nothing later swamps that difference)."""
+    c = synth.make_case("contract", T=T, H=H, K=1, R=R, E=8, act_dtype=act, rsf=float(np.float32(1.0 / 3.0)),
+                        shared=True, gemm2_std=1.0)
+    for r in range(R):
+        c.scale[r] = torch.ones_like(c.scale[r])
+        rows = c.gemm2[r].double()[c.perm[r][:, 0].long()]  # 16-bit x 24-bit product: exact in FP64
+        c.shared[r] = (-(rows * c.rsf)).to(act)
+    c.residual = torch.zeros_like(c.residual)
+    return c

@@ -523,6 +523,23 @@ def all_pins():
     return failed
 
 
+def test_contraction_case_is_discriminating(tmp_path):
+    """The crafted case of the GPU contraction test must change under a fused shared-row step."""
+    from helpers import contraction_case
+    old = "acc = acc * a->rsf;\n          if (P->shared) acc = acc + act_load(P->shared, (int64_t)t * H + h, dt);"
+    new = "acc = P->shared ? fmaf(acc, a->rsf, act_load(P->shared, (int64_t)t * H + h, dt)) : acc * a->rsf;"
+    src = oracle.source()
+    assert src.count(old) == 1
+    path = oracle.build_variant(src.replace(old, new), str(tmp_path / "libfused.so"))
+    for act in (torch.bfloat16, torch.float16):
+        case = contraction_case(act)
+        want = oracle.finalize(case)["residual_out"]
+        with oracle.use_library(path):
+            fused = oracle.finalize(case)["residual_out"]
+        frac = np.mean(fused != want)
+        assert frac > 0.05, f"{act}: only {frac:.4f} of the outputs tell the fused step apart"
+
+
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
 def test_mutant_is_caught(mutant, tmp_path):
     old, new = MUTANTS[mutant]
