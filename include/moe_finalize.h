@@ -145,8 +145,9 @@ typedef struct {
   int32_t cluster;    /* CTAs per cluster (1 = no cluster)                                           */
   int32_t block;      /* threads per CTA                                                             */
   int32_t smem_bytes; /* dynamic shared memory per CTA                                               */
-  int32_t chunk;      /* stream kernel: hidden elements per pipeline stage; cluster kernel: slice   */
-  int32_t stages;     /* stream kernel: pipeline depth; cluster kernel: 1                           */
+  int32_t chunk;      /* stream kernel: hidden elements per pipeline stage; cluster kernel: hidden   */
+                      /* elements per chunk of a CTA                                                */
+  int32_t stages;     /* stream kernel: pipeline depth; cluster kernel: chunks per CTA               */
 } mfr_plan;
 
 /* Enqueue the fused finalize.  Returns MFR_OK or a negative status (see above).

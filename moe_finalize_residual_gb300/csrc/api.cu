@@ -155,43 +155,50 @@ void fill_params(const mfr_args* a, KParams* p) {
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
-int pow2_ceil(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
-}
-
-// Token count up to which the cluster kernel is chosen automatically, and the stream kernel's shape
-// (probe builds may override them).
+// Token count up to which the cluster kernel is chosen automatically (measured on GB300 at H=6144,
+// top-8, R=4: the cluster kernel is ahead up to 512 tokens, the stream kernel from about 1024), and
+// the cluster planner's targets (probe builds may override them).
 #ifndef MFR_CLUSTER_MAX_TOKENS
-#define MFR_CLUSTER_MAX_TOKENS 96
+#define MFR_CLUSTER_MAX_TOKENS 512
 #endif
 #ifndef MFR_CLUSTER_BLOCK
 #define MFR_CLUSTER_BLOCK 512
 #endif
+#ifndef MFR_CLUSTER_CTAS_PER_SM
+#define MFR_CLUSTER_CTAS_PER_SM 2
+#endif
+#ifndef MFR_CLUSTER_MAX_SIZE
+#define MFR_CLUSTER_MAX_SIZE 16
+#endif
 constexpr int kClusterMaxTokens = MFR_CLUSTER_MAX_TOKENS;
-constexpr int kMaxCluster = 16;
+constexpr int kMaxCluster = MFR_CLUSTER_MAX_SIZE;
 
-// Cluster kernel: C CTAs per token, each holding SV 16-byte vectors of the hidden row for all R
-// partials (R*SV threads).  SV comes from the parallelism target (about two CTAs per SM over the batch),
-// capped by the preferred CTA size, and bounded so that C <= 16 and R*SV <= kClusterMaxThreads.
+// Cluster kernel: C CTAs per token, each covering NCH chunks of SV 16-byte vectors of the hidden row
+// for all R partials (R*SV threads).  C comes from the parallelism target (about two CTAs per SM over
+// the batch), SV is capped by the preferred CTA size, and NCH covers the rest of the row; C <= 16 and
+// R*SV <= kClusterMaxThreads.
 bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
   const int nvec = a->H / 8;
   const int unit = (a->H % 16 == 0) ? 2 : 1;  // slices start on 16-element blocks when H allows
   const int R = a->R;
   const int sv_max = (kClusterMaxThreads / R) / unit * unit;
-  const int sv_min = align_up(ceil_div(nvec, kMaxCluster), unit);
-  if (sv_min > sv_max) return false;
-  const int c_target = std::min(kMaxCluster, pow2_ceil(ceil_div(2 * d.sms, std::max(1, a->T))));
-  const int sv_soft = std::max(unit, (MFR_CLUSTER_BLOCK / R) / unit * unit);
-  int sv = align_up(ceil_div(nvec, c_target), unit);
-  sv = std::min(sv, std::max(sv_soft, sv_min));
-  sv = std::min(std::max(sv, sv_min), sv_max);
-  for (; sv <= sv_max; sv = std::min(sv_max + unit, align_up(sv * 2, unit))) {
-    const int C = ceil_div(nvec, sv);
-    const int block = align_up(sv * R, 32);
-    const int off_red = align_up((R + 2) * sv * 16, 16);
-    const int smem = align_up(off_red + 34 * 4, 16);
+  const int sv_soft = std::min(sv_max, std::max(unit, (MFR_CLUSTER_BLOCK / R) / unit * unit));
+  // About two CTAs per SM in all: c_goal CTAs per token, each covering nchunk chunks of sv vectors.
+  // Few tokens: one chunk, the row spread over up to kMaxCluster CTAs.  More tokens: fewer CTAs per
+  // token, each looping over several chunks.  More CTAs per token when shared memory is short.
+  // Cluster sizes of 5-7 and 9-15 CTAs measured slower than the next smaller size in {1, 2, 3, 4, 8, 16}.
+  const int c_raw = std::max(1, std::min(kMaxCluster, (MFR_CLUSTER_CTAS_PER_SM * d.sms) / std::max(1, a->T)));
+  const int c_goal = c_raw >= 16 ? 16 : c_raw >= 8 ? 8 : c_raw >= 4 ? 4 : c_raw;
+  for (int cg = c_goal; cg <= kMaxCluster; ++cg) {
+    const int sv = std::min(sv_soft, align_up(ceil_div(nvec, cg), unit));
+    const int nch = ceil_div(nvec, cg * sv);
+    const int C = ceil_div(nvec, nch * sv);
+    if (C > kMaxCluster) return false;
+    const int sv_fit = align_up(ceil_div(nvec, C * nch), unit);  // even slices
+    const int block = align_up(sv_fit * R, 32);
+    const int off_red = align_up((R + 2) * nch * sv_fit * 16, 16);
+    const int off_routes = align_up(off_red + 34 * 4, 16);
+    const int smem = align_up(off_routes + R * a->K * 8, 16);
     if (smem > d.smem_optin) continue;
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
     if (C > 1) {
@@ -209,8 +216,10 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
       }
       if (n < 1) continue;
     }
-    p->slice_vec = sv;
+    p->slice_vec = sv_fit;
+    p->nchunk = nch;
     p->off_red = off_red;
+    p->off_routes = off_routes;
     *g = geo;
     return true;
   }
@@ -348,8 +357,8 @@ int moe_finalize_plan(const mfr_args* args, mfr_plan* plan) {
   plan->cluster = g.cluster;
   plan->block = g.block;
   plan->smem_bytes = g.smem;
-  plan->chunk = kernel == MFR_KERNEL_STREAM ? p.chunk : p.slice_vec * 8;  // cluster: hidden elements per CTA
-  plan->stages = kernel == MFR_KERNEL_STREAM ? p.stages : 1;
+  plan->chunk = kernel == MFR_KERNEL_STREAM ? p.chunk : p.slice_vec * 8;  // cluster: hidden elements per chunk
+  plan->stages = kernel == MFR_KERNEL_STREAM ? p.stages : p.nchunk;     // cluster: chunks per CTA
   return MFR_OK;
 }
 

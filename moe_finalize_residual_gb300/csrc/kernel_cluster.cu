@@ -1,19 +1,23 @@
 // Small-batch fused finalize: one thread-block cluster per token, the hidden dimension split into
-// equal slices, one slice per CTA of the cluster.
+// equal slices, one slice per CTA of the cluster; a CTA covers its slice in one or more chunks.
 //
 // Design (prior art: flashinfer PR #6546, finalizeKernelSmallBatch, Description -- one CTA per
 // (token, hidden slice), 128-bit loads, top-K work split over thread groups combined through shared
 // memory, PDL trigger at kernel start; flashinfer PR #6631, Description -- load the indices and
 // scales of the routes first, then all rows, so the row loads are in flight together):
 //
-//  * a CTA holds SV 16-byte vectors of the token's hidden row; its threads form R groups of SV, one
-//    group per partial: thread (r, v) owns vector v of partial r;
+//  * a CTA covers NCH chunks of SV 16-byte vectors of the token's hidden row; its threads form R groups
+//    of SV, one group per partial: thread (r, v) owns vector v of each chunk of partial r.  With few
+//    tokens a CTA holds one chunk and the row is spread over up to 16 CTAs; with more tokens fewer
+//    CTAs per token loop over several chunks, so the grid stays about two CTAs per SM in one wave;
 //  * each thread reads the route indices and scales of its partial (the same addresses for the whole
 //    warp), then issues all its rows as 128-bit loads at once (up to KC in flight; K > KC repeats),
 //    plus its shared-expert row, and runs the FP32 fused multiply-add chain over them in route order:
 //    every partial row is produced by one thread in the definition's order, so it is bit-exact;
-//  * each group writes its rounded partial row to shared memory; group 0 sums the R rows in rank order
-//    (the shared-memory combine), adds the residual and writes residual_out;
+//  * the shared-expert, residual and gamma slices of every chunk are copied into shared memory first;
+//    each group writes its rounded partial rows to shared memory (one buffer per chunk, so one barrier
+//    serves all chunks); group 0 sums the R rows in rank order (the shared-memory combine), adds the
+//    residual and writes residual_out, keeping it in shared memory for the epilogue;
 //  * the sum of squares is reduced with warp shuffles, then across warps in shared memory, then across
 //    the cluster's CTAs through distributed shared memory in CTA-rank order, so every CTA gets the same
 //    deterministic total; group 0 then writes norm_out and the quantised output.
@@ -25,42 +29,44 @@
 
 namespace mfr {
 
-// Route indices and scales of routes k0..k0+KC-1 of partial P for token t; idx < 0 marks a route to
-// skip (flashinfer PR #6631, Test changes: -1 routes contribute nothing; one bound check per route).
-template <int KC>
-__device__ __forceinline__ void load_routes(const KParams& p, const KPartial& P, int t, int k0, bool on,
-                                            int idx[KC], float sc[KC]) {
-#pragma unroll
-  for (int j = 0; j < KC; ++j) {
-    idx[j] = -1;
-    sc[j] = 0.0f;
-    const int k = k0 + j;
-    if (on && k < p.K) {
-      const int64_t e = static_cast<int64_t>(t) * p.K + k;
-      const int32_t ix = P.perm[e];
-      if (ix >= 0 && static_cast<int64_t>(ix) < P.rows) {
-        idx[j] = ix;
-        sc[j] = load_scale(P.scale, e, p.scale_dtype);
-      }
-    }
+// The token's route table for partial P: entry k holds the row index of route k, or -1 for a route to
+// skip (flashinfer PR #6631, Test changes: -1 routes contribute nothing; one bound check per route),
+// and the bits of its scale.  Thread v of the partial's group fills entries v, v + SV, ...
+__device__ __forceinline__ void fill_routes(const KParams& p, const KPartial& P, int t, int v, int SV, int2* rt) {
+  for (int k = v; k < p.K; k += SV) {
+    const int64_t e = static_cast<int64_t>(t) * p.K + k;
+    const int32_t ix = P.perm[e];
+    const float sc = load_scale(P.scale, e, p.scale_dtype);  // independent of the index: both loads in flight
+    const bool ok = ix >= 0 && static_cast<int64_t>(ix) < P.rows;
+    rt[k] = make_int2(ok ? ix : -1, ok ? __float_as_int(sc) : 0);
   }
 }
 
-// All KC rows in flight together, then the FMA chain over them in route order.
+// Routes k0..k0+KC-1 of the table, all KC rows in flight together, then the FMA chain over them in
+// route order (rows of routes with index -1 are neither loaded nor added).  A route's table entry is
+// read again for its FMA, so the indices and scales need no registers while the loads are in flight.
 template <typename A, int KC>
-__device__ __forceinline__ void gather_chain(const KPartial& P, int H, int vec, const int idx[KC],
-                                             const float sc[KC], float acc[8]) {
+__device__ __forceinline__ void gather_chain(const KPartial& P, int H, int K, int vec, const int2* rt, int k0,
+                                             float acc[8]) {
   uint4 d[KC];
 #pragma unroll
-  for (int j = 0; j < KC; ++j)
-    if (idx[j] >= 0) d[j] = ldg16(P.gemm2 + (static_cast<int64_t>(idx[j]) * H + vec * 8) * 2);
+  for (int j = 0; j < KC; ++j) {
+    const int ix = (k0 + j < K) ? rt[k0 + j].x : -1;
+    if (ix >= 0) d[j] = ldg16(P.gemm2 + (static_cast<int64_t>(ix) * H + vec * 8) * 2);
+  }
+  const uint32_t rt_s = smem_addr(rt + k0);
 #pragma unroll
   for (int j = 0; j < KC; ++j) {
-    if (idx[j] >= 0) {
-      float x[8];
-      unpack8<A>(d[j], x);
+    if (k0 + j < K) {
+      int ix, scb;
+      asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(ix), "=r"(scb) : "r"(rt_s + 8u * j) : "memory");
+      if (ix >= 0) {
+        float x[8];
+        unpack8<A>(d[j], x);
+        const float sc = __int_as_float(scb);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(sc[j], x[i], acc[i]);
+        for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(sc, x[i], acc[i]);
+      }
     }
   }
 }
@@ -77,87 +83,98 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
   const int SV = p.slice_vec;
+  const int NCH = p.nchunk;
   const uint32_t C = cluster_nctarank();
   const uint32_t crank = cluster_ctarank();
   const int t = static_cast<int>(blockIdx.x / C);
   const int H = p.H;
+  const int nvec = H >> 3;
   const int r = tid / SV;                       // partial of this thread's group
   const int v = tid - r * SV;
-  const int vec = static_cast<int>(crank) * SV + v;  // 16-byte vector of the hidden row
+  const int vec0 = static_cast<int>(crank) * NCH * SV + v;  // chunk ch holds vector vec0 + ch * SV
   const bool in_group = r < p.R;
-  const bool active = in_group && vec < (H >> 3);
-  uint4* xch = reinterpret_cast<uint4*>(smem);                // [R][SV] shared rows, then partial rows
-  uint4* res_s = xch + p.R * SV;                              // [SV] residual slice
-  uint4* gam_s = res_s + SV;                                  // [SV] gamma slice
+  const bool any = in_group && vec0 < nvec;     // the thread has a vector in chunk 0 (so it has work)
+  uint4* xch = reinterpret_cast<uint4*>(smem);                // [NCH][R][SV] shared rows, then partial rows
+  uint4* res_s = xch + NCH * p.R * SV;                        // [NCH][SV] residual slices, then residual_out
+  uint4* gam_s = res_s + NCH * SV;                            // [NCH][SV] gamma slices
   float* red = reinterpret_cast<float*>(smem + p.off_red);    // [32] warp sums, [32] CTA sum, [33] total
   const KPartial& P = p.part[in_group ? r : 0];
   const bool has_shared = in_group && ((p.shared_mask >> r) & 1u);
-  const bool lead = (r == 0) && active;         // group 0 finishes the token
+  const bool lead_group = r == 0;               // group 0 finishes the token
 
-  int idx[KC];
-  float sc[KC];
+  int2* rt = reinterpret_cast<int2*>(smem + p.off_routes) + (in_group ? r : 0) * p.K;  // this partial's routes
   if (p.pdl) pdl_launch_dependents();
-  if (p.routing_early) load_routes<KC>(p, P, t, 0, active, idx, sc);
+  if (p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
   if (p.pdl) pdl_wait();
-  if (!p.routing_early) load_routes<KC>(p, P, t, 0, active, idx, sc);
+  if (!p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
 
-  // Rows that do not depend on the routing go out first, straight into shared memory (each thread
-  // later reads only what it copied itself, after waiting for its own copies).
-  if (has_shared && active)
-    cp_async16(smem_addr(&xch[r * SV + v]), P.shared + (static_cast<int64_t>(t) * H + vec * 8) * 2);
-  if (lead) {
-    cp_async16(smem_addr(&res_s[v]), p.residual + (static_cast<int64_t>(t) * H + vec * 8) * 2);
-    cp_async16(smem_addr(&gam_s[v]), p.gamma + static_cast<int64_t>(vec) * 16);
+  // Rows that do not depend on the routing go out first, every chunk's, straight into shared memory
+  // (each thread later reads only what it copied itself, after waiting for its own copies).
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int vec = vec0 + ch * SV;
+    if (!in_group || vec >= nvec) break;
+    const int64_t off = (static_cast<int64_t>(t) * H + vec * 8) * 2;
+    if (has_shared) cp_async16(smem_addr(&xch[(ch * p.R + r) * SV + v]), P.shared + off);
+    if (lead_group) {
+      cp_async16(smem_addr(&res_s[ch * SV + v]), p.residual + off);
+      cp_async16(smem_addr(&gam_s[ch * SV + v]), p.gamma + static_cast<int64_t>(vec) * 16);
+    }
   }
   cp_async_commit();
+  __syncthreads();  // the route table is written
 
-  float acc[8];
+  // Each chunk: the partial's FMA chain over its routes, times the routed scaling factor, plus the
+  // shared row, rounded once (the partial row p_r), into the chunk's exchange buffer.
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int vec = vec0 + ch * SV;
+    if (!in_group || vec >= nvec) break;
+    float acc[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  if (active) {
-    gather_chain<A, KC>(P, H, vec, idx, sc, acc);
-    for (int k0 = KC; k0 < p.K; k0 += KC) {
-      load_routes<KC>(p, P, t, k0, true, idx, sc);
-      gather_chain<A, KC>(P, H, vec, idx, sc, acc);
-    }
-    // times the routed scaling factor, plus the shared row, rounded once (the partial row p_r)
-    cp_async_wait_all();
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain<A, KC>(P, H, p.K, vec, rt, k0, acc);
+    if (ch == 0) cp_async_wait_all();
+    uint4* xr = &xch[(ch * p.R + r) * SV + v];
     float shv[8];
-    unpack8<A>(xch[r * SV + v], shv);
+    unpack8<A>(*xr, shv);
     float a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       a[i] = __fmul_rn(acc[i], p.rsf);
       if (has_shared) a[i] = __fadd_rn(a[i], shv[i]);
     }
-    xch[r * SV + v] = make_uint4(Act<A>::pack(a[0], a[1]), Act<A>::pack(a[2], a[3]), Act<A>::pack(a[4], a[5]),
-                                 Act<A>::pack(a[6], a[7]));
+    *xr = make_uint4(Act<A>::pack(a[0], a[1]), Act<A>::pack(a[2], a[3]), Act<A>::pack(a[4], a[5]),
+                     Act<A>::pack(a[6], a[7]));
   }
   cp_async_wait_all();
   __syncthreads();
 
-  // Group 0: rank sum in order 0..R-1, residual add, sum of squares.
-  float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // Group 0, chunk by chunk: rank sum in order 0..R-1, residual add (kept in place of the residual
+  // slice for the epilogue), sum of squares.
   float ss = 0.0f;
-  if (lead) {
-    float S[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int rr = 0; rr < p.R; ++rr) {
-      float pr[8];
-      unpack8<A>(xch[rr * SV + v], pr);
+  if (lead_group) {
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int vec = vec0 + ch * SV;
+      if (vec >= nvec) break;
+      float S[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int rr = 0; rr < p.R; ++rr) {
+        float pr[8];
+        unpack8<A>(xch[(ch * p.R + rr) * SV + v], pr);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) S[i] = __fadd_rn(S[i], pr[i]);
-    }
-    float res[8];
-    unpack8<A>(res_s[v], res);
+        for (int i = 0; i < 8; ++i) S[i] = __fadd_rn(S[i], pr[i]);
+      }
+      float res[8], x[8];
+      unpack8<A>(res_s[ch * SV + v], res);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[i] = Act<A>::round(__fadd_rn(Act<A>::round(S[i]), res[i]));
-      ss = __fmaf_rn(x[i], x[i], ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
+      for (int i = 0; i < 8; ++i) {
+        x[i] = Act<A>::round(__fadd_rn(Act<A>::round(S[i]), res[i]));
+        ss = __fmaf_rn(x[i], x[i], ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
+      }
+      const uint4 ro = make_uint4(Act<A>::pack(x[0], x[1]), Act<A>::pack(x[2], x[3]), Act<A>::pack(x[4], x[5]),
+                                  Act<A>::pack(x[6], x[7]));
+      res_s[ch * SV + v] = ro;
+      if (p.residual_out != nullptr)
+        *reinterpret_cast<uint4*>(p.residual_out + (static_cast<int64_t>(t) * H + vec * 8) * 2) = ro;
     }
-    if (p.residual_out != nullptr)
-      *reinterpret_cast<uint4*>(p.residual_out + (static_cast<int64_t>(t) * H + vec * 8) * 2) =
-          make_uint4(Act<A>::pack(x[0], x[1]), Act<A>::pack(x[2], x[3]), Act<A>::pack(x[4], x[5]),
-                     Act<A>::pack(x[6], x[7]));
   }
 
   // Sum of squares: warp shuffle, warps in order, then the cluster's CTAs in rank order.
@@ -186,9 +203,14 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   const float rstd = rms_rstd(red[33], H, p.eps);
   if (tid < ((SV + 31) & ~31)) {  // the warps that hold group 0 (whole warps, for the NVFP4 shuffles)
     const float qscale = (p.quant != MFR_QUANT_NONE) ? *p.quant_scale : 1.0f;
-    float g[8];
-    unpack8<A>(lead ? gam_s[v] : make_uint4(0, 0, 0, 0), g);
-    epilogue<A, 8>(p, t, vec * 8, lead, x, g, rstd, qscale);
+    for (int ch = 0; ch < NCH; ++ch) {  // the same trip count for the whole warp
+      const int vec = vec0 + ch * SV;
+      const bool lead = lead_group && vec < nvec;
+      float x[8], g[8];
+      unpack8<A>(lead ? res_s[ch * SV + v] : make_uint4(0, 0, 0, 0), x);
+      unpack8<A>(lead ? gam_s[ch * SV + v] : make_uint4(0, 0, 0, 0), g);
+      epilogue<A, 8>(p, t, vec * 8, lead, x, g, rstd, qscale);
+    }
   }
   if (C > 1) cluster_wait_acquire();  // no CTA leaves while a peer may still read its shared memory
 }

@@ -54,7 +54,9 @@ struct KParams {
   int32_t routing_early;  // routing may be read before the dependency wait
   float rsf, eps;
   // cluster kernel
-  int32_t slice_vec;      // 16-byte vectors of hidden per CTA (the last CTA may hold fewer)
+  int32_t slice_vec;      // cluster kernel: 16-byte vectors per CTA per chunk (the last CTA may hold fewer)
+  int32_t nchunk;         // cluster kernel: chunks of slice_vec vectors per CTA
+  int32_t off_routes;     // cluster kernel: shared-memory route table [R][K] (row index or -1, scale)
   int32_t off_red;
   // stream kernel
   int32_t chunk;          // hidden elements per pass

@@ -227,6 +227,35 @@ def test_max_slots(kernel):
     check_case(case, kernel)
 
 
+@pytest.mark.parametrize("T,H,R,K,act", [(40, 6144, 4, 8, torch.bfloat16), (96, 6144, 4, 8, torch.float16),
+                                          (200, 7168, 2, 10, torch.bfloat16), (512, 6144, 4, 8, torch.bfloat16),
+                                          (300, 4096, 1, 32, torch.bfloat16), (64, 32768, 8, 4, torch.float16)])
+def test_cluster_chunks(T, H, R, K, act):
+    """The cluster kernel with several chunks per CTA (medium batches), sampled tokens at the larger sizes."""
+    import moe_finalize_residual_gb300 as mfr
+    case = synth.make_case("chunks", T=T, H=H, K=K, R=R, E=64, act_dtype=act, rsf=2.5, shared=True,
+                           mask_quarter=True, device="cuda")
+    plan = mfr.moe_finalize_plan(partials_of(case), case.residual, case.gamma, kernel="cluster")
+    assert plan["kernel"] == "cluster" and plan["stages"] >= 1
+    toks = _sample_tokens(T) if T > 64 else np.arange(T)
+    sub = subcase(case, toks)
+    res = run(case, kernel="cluster")
+    assert res.guards_ok
+    check_against_oracle(sub, res, oracle.finalize(sub), tokens=toks)
+
+
+def test_cluster_plans_use_chunks():
+    """Medium batches give fewer CTAs per token, each covering several chunks, in one wave."""
+    import moe_finalize_residual_gb300 as mfr
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for T in (64, 128, 256, 512):
+        case = synth.make_case("p", T=T, H=6144, K=8, R=4, E=64, shared=True, device="cuda")
+        plan = mfr.moe_finalize_plan(partials_of(case), case.residual, case.gamma)
+        assert plan["kernel"] == "cluster", plan
+        assert plan["stages"] >= 2 and plan["cluster"] * plan["stages"] * plan["chunk"] >= 6144, plan
+        assert plan["grid"] == T * plan["cluster"] and plan["grid"] <= max(2 * sms, T), plan
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_single_route_identity(kernel):
     case = synth.make_case("id", T=9, H=512, K=1, R=1, E=8, scale_dtype=None, rsf=1.0)
