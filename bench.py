@@ -155,14 +155,16 @@ def make_sets(T, nsets, device, base=HEADLINE):
                                                                            + 7919 * i}) for i in range(nsets)]
 
 
-def finalize_fn(mfr, case, outs, quant="none", qscale=None, sf_layout="row_major", kernel="auto"):
+def finalize_fn(mfr, case, outs, quant="none", qscale=None, sf_layout="row_major", kernel="auto",
+                routing_ready=False):
     parts = [mfr.Partial(case.gemm2[r], case.perm[r], case.scale[r], case.shared[r]) for r in range(case.R)]
 
     def call():
         mfr.moe_finalize_fused(parts, case.residual, case.gamma, routed_scaling_factor=case.rsf, eps=case.eps,
                                residual_out=outs[0], norm_out=outs[1], want_residual_out=outs[0] is not None,
                                want_norm_out=outs[1] is not None, quant_mode=quant, quant_scale=qscale,
-                               sf_layout=sf_layout, quant_out=outs[2], sf_out=outs[3], pdl=True, kernel=kernel,
+                               sf_layout=sf_layout, quant_out=outs[2], sf_out=outs[3], pdl=True,
+                               routing_ready=routing_ready, kernel=kernel,
                                check=False)
     return call
 
@@ -248,6 +250,30 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_case(spec: str, reps: int):
+    """One workload, launched `reps` times back to back (no graph, no timing): the profiler's target."""
+    parts = spec.split(":")
+    family, T = parts[0], int(parts[1])
+    H = int(parts[2]) if len(parts) > 2 and parts[2] else None
+    quant = parts[3] if len(parts) > 3 and parts[3] else "none"
+    kernel = parts[4] if len(parts) > 4 and parts[4] else "auto"
+    import moe_finalize_residual_gb300 as mfr
+    torch.cuda.set_device(0)
+    base = dict(HEADLINE) if family == "decode" else {k: v for k, v in synth.CONFIGS[family].items() if k != "Ts"}
+    if H:
+        base["H"] = H
+    c = synth.make_case(f"{family}-T{T}", T=T, device="cuda", **base)
+    o, qs = alloc_outs(mfr, c, quant)
+    fn = finalize_fn(mfr, c, o, quant, qs, kernel=kernel)
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    p = mfr.moe_finalize_plan([mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r]) for r in range(c.R)],
+                              c.residual, c.gamma, kernel=kernel)
+    print(json.dumps({"case": spec, "launches": reps, "algorithmic_bytes_per_launch": algorithmic_bytes(c, quant),
+                      "plan": p}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -255,8 +281,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="headline only (no sweep, bandwidth, e2e, cpu)")
+    ap.add_argument("--case", default=None, metavar="FAMILY:T[:H[:QUANT[:KERNEL]]]",
+                    help="run one workload --steps times without timing (for profilers), e.g. decode:128 or "
+                         "bandwidth:1024:7168:none:stream")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.case:
+        run_case(args.case, args.steps)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -335,11 +367,19 @@ def main():
         floor_pdl, _ = time_graph(gf, 50, 5)
         gf2 = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=False))
         floor_nopdl, _ = time_graph(gf2, 50, 5)
-        del gf, gf2
+        # the dependent index -> row -> store chain alone (20 rows, one per launch: L2-warm like the sweep)
+        rows = torch.zeros(1024, 6144, dtype=torch.bfloat16, device=dev)
+        gidx = torch.randint(0, rows.shape[0], (GRAPH_LAUNCHES, 1), dtype=torch.int32, device=dev)
+        gout = torch.empty(512, dtype=torch.uint8, device=dev)
+        gf3 = capture_graph(lambda i: mfr.moe_finalize_gather_floor_launch(gidx[i], rows, gout, pdl=True))
+        floor_gather, _ = time_graph(gf3, 50, 5)
+        del gf, gf2, gf3, rows
         for s in sweep:
             s["x_floor"] = round(s["us"] / floor_pdl, 2)
+            s["x_gather_floor"] = round(s["us"] / floor_gather, 2)
         extras["sweep_l2_warm"] = sweep
-        extras["launch_floor_us"] = {"pdl": round(floor_pdl, 3), "no_pdl": round(floor_nopdl, 3)}
+        extras["launch_floor_us"] = {"pdl": round(floor_pdl, 3), "no_pdl": round(floor_nopdl, 3),
+                                     "gather_chain_pdl": round(floor_gather, 3)}
         del sets, outs, calls
         torch.cuda.empty_cache()
 

@@ -178,6 +178,16 @@ const char* moe_finalize_last_error(void);
  * back-to-back launches is the launch floor the finalize is compared against. */
 int moe_finalize_empty_launch(struct CUstream_st* stream, uint32_t flags);
 
+/* Measurement aid (no counterpart on the pages): enqueue one CTA of 32 threads that reads idx[0] (a
+ * device int32), then 16 bytes per thread of row idx[0] of `rows` (nrows rows of row_bytes bytes, a
+ * device buffer), and writes those 512 bytes to `out` (device, at least 512 bytes): the dependent
+ * index -> row -> store chain every finalize begins with, launched like the finalize (PDL attribute
+ * iff flags has MFR_FLAG_PDL).  An index outside [0, nrows) writes nothing.  Buffers and row_bytes
+ * must be 16-byte aligned and row_bytes >= 512 (else MFR_ERR_INVALID_ARG).  Its time in a graph of
+ * back-to-back launches is the latency floor of a gather (launch plus two dependent memory reads). */
+int moe_finalize_gather_floor_launch(const int32_t* idx, const void* rows, int64_t nrows, int64_t row_bytes,
+                                     void* out, struct CUstream_st* stream, uint32_t flags);
+
 /* Robustness aid (no counterpart on the pages): the stream kernel bounds every wait on its own
  * pipeline barriers (about 2 s); a wait that runs out records a count on the device and the kernel
  * returns early.  This reads the count for the current device into *count and resets it.  It

@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "Partial", "moe_finalize_fused", "moe_finalize_plan", "moe_finalize_sf_bytes", "moe_finalize_quant_bytes",
-    "moe_finalize_empty_launch", "moe_finalize_read_timeouts", "moe_finalize_abi_version", "library_path",
+    "moe_finalize_empty_launch", "moe_finalize_gather_floor_launch", "moe_finalize_read_timeouts", "moe_finalize_abi_version", "library_path",
     "QUANT", "SF_LAYOUT", "KERNEL", "MFR_FLAG_PDL", "MFR_FLAG_ROUTING_READY",
 ]
 
@@ -83,6 +83,8 @@ def _load_library():
     lib.moe_finalize_last_error.restype = ctypes.c_char_p
     lib.moe_finalize_empty_launch.argtypes = [P, ctypes.c_uint32]
     lib.moe_finalize_empty_launch.restype = ctypes.c_int
+    lib.moe_finalize_gather_floor_launch.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, P, P, ctypes.c_uint32]
+    lib.moe_finalize_gather_floor_launch.restype = ctypes.c_int
     lib.moe_finalize_read_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.moe_finalize_read_timeouts.restype = ctypes.c_int
     lib.moe_finalize_abi_version.argtypes = []
@@ -280,6 +282,20 @@ def moe_finalize_quant_bytes(T: int, H: int, quant_mode="fp8") -> int:
 def moe_finalize_empty_launch(stream: Optional[torch.cuda.Stream] = None, pdl: bool = True):
     s = stream if stream is not None else torch.cuda.current_stream()
     _check(_lib.moe_finalize_empty_launch(ctypes.c_void_p(s.cuda_stream), MFR_FLAG_PDL if pdl else 0))
+
+
+def moe_finalize_gather_floor_launch(idx: torch.Tensor, rows: torch.Tensor, out: torch.Tensor,
+                                     stream: Optional[torch.cuda.Stream] = None, pdl: bool = True):
+    """The index -> row -> store chain alone (a latency floor for the finalize); see the C header."""
+    if idx.dtype != torch.int32 or not (idx.is_cuda and rows.is_cuda and out.is_cuda):
+        raise MoEFinalizeError("idx must be a CUDA int32 tensor; rows and out CUDA tensors")
+    if not rows.is_contiguous() or rows.dim() != 2 or out.numel() * out.element_size() < 512:
+        raise MoEFinalizeError("rows must be a contiguous 2-D tensor and out at least 512 bytes")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(_lib.moe_finalize_gather_floor_launch(
+        ctypes.c_void_p(idx.data_ptr()), ctypes.c_void_p(rows.data_ptr()), rows.shape[0],
+        rows.shape[1] * rows.element_size(), ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(s.cuda_stream),
+        MFR_FLAG_PDL if pdl else 0))
 
 
 def moe_finalize_read_timeouts() -> int:

@@ -197,7 +197,7 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
     const int sv_fit = align_up(ceil_div(nvec, C * nch), unit);  // even slices
     const int block = align_up(sv_fit * R, 32);
     const int off_red = align_up((R + 2) * nch * sv_fit * 16, 16);
-    const int off_routes = align_up(off_red + 34 * 4, 16);
+    const int off_routes = align_up(off_red + 50 * 4, 16);
     const int smem = align_up(off_routes + R * a->K * 8, 16);
     if (smem > d.smem_optin) continue;
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
@@ -326,6 +326,20 @@ __global__ void empty_kernel(int pdl) {
   }
 }
 
+// The dependent chain every finalize starts with, alone: read a route index, then 16 bytes per lane of
+// the row it names, then write them.
+__global__ void gather_floor_kernel(const int32_t* idx, const uint8_t* rows, int64_t nrows, int64_t row_bytes,
+                                    uint8_t* out, int pdl) {
+  if (pdl) {
+    pdl_launch_dependents();
+    pdl_wait();
+  }
+  const int32_t i = idx[0];
+  const int64_t off = static_cast<int64_t>(threadIdx.x) * 16;
+  if (i >= 0 && i < nrows && off + 16 <= row_bytes)
+    *reinterpret_cast<uint4*>(out + off) = *reinterpret_cast<const uint4*>(rows + i * row_bytes + off);
+}
+
 }  // namespace
 }  // namespace mfr
 
@@ -407,6 +421,27 @@ int moe_finalize_empty_launch(struct CUstream_st* stream, uint32_t flags) {
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, empty_kernel, pdl);
   if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "empty launch: %s", cudaGetErrorString(e));
+  return MFR_OK;
+}
+
+int moe_finalize_gather_floor_launch(const int32_t* idx, const void* rows, int64_t nrows, int64_t row_bytes,
+                                     void* out, struct CUstream_st* stream, uint32_t flags) {
+  if (idx == nullptr || rows == nullptr || out == nullptr || nrows <= 0 || row_bytes < 512 ||
+      (reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(out) | static_cast<uintptr_t>(row_bytes)) % 16)
+    return fail(MFR_ERR_INVALID_ARG, "gather floor: non-null 16-byte aligned buffers, rows of at least 512 bytes");
+  const int pdl = (flags & MFR_FLAG_PDL) ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gather_floor_kernel, idx, static_cast<const uint8_t*>(rows), nrows,
+                                     row_bytes, static_cast<uint8_t*>(out), pdl);
+  if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "gather floor launch: %s", cudaGetErrorString(e));
   return MFR_OK;
 }
 

@@ -19,8 +19,9 @@
 //    serves all chunks); group 0 sums the R rows in rank order (the shared-memory combine), adds the
 //    residual and writes residual_out, keeping it in shared memory for the epilogue;
 //  * the sum of squares is reduced with warp shuffles, then across warps in shared memory, then across
-//    the cluster's CTAs through distributed shared memory in CTA-rank order, so every CTA gets the same
-//    deterministic total; group 0 then writes norm_out and the quantised output.
+//    the cluster's CTAs: each CTA writes its sum into a slot of every peer's shared memory, and after
+//    one cluster barrier every CTA adds the slots in rank order, so all get the same deterministic
+//    total; group 0 then writes residual_out, norm_out and the quantised output.
 //
 // No CTA waits on a flag in global memory; the only cross-CTA synchronisation is the hardware cluster
 // barrier, which every CTA reaches unconditionally.
@@ -97,19 +98,24 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   uint4* xch = reinterpret_cast<uint4*>(smem);                // [NCH][R][SV] shared rows, then partial rows
   uint4* res_s = xch + NCH * p.R * SV;                        // [NCH][SV] residual slices, then residual_out
   uint4* gam_s = res_s + NCH * SV;                            // [NCH][SV] gamma slices
-  float* red = reinterpret_cast<float*>(smem + p.off_red);    // [32] warp sums, [32] CTA sum, [33] total
+  float* red = reinterpret_cast<float*>(smem + p.off_red);    // [0,32) warp sums, [32] CTA sum, [33] total,
+                                                              // [34,50) the cluster's CTA sums by rank
   const KPartial& P = p.part[in_group ? r : 0];
   const bool has_shared = in_group && ((p.shared_mask >> r) & 1u);
   const bool lead_group = r == 0;               // group 0 finishes the token
 
+  // Every CTA of the cluster arrives here on entry; the matching wait comes before the first write into
+  // a peer's shared memory, so no CTA writes into one that has not started.
+  if (C > 1) cluster_arrive_relaxed();
   int2* rt = reinterpret_cast<int2*>(smem + p.off_routes) + (in_group ? r : 0) * p.K;  // this partial's routes
   if (p.pdl) pdl_launch_dependents();
   if (p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
   if (p.pdl) pdl_wait();
   if (!p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
 
-  // Rows that do not depend on the routing go out first, every chunk's, straight into shared memory
-  // (each thread later reads only what it copied itself, after waiting for its own copies).
+  // Rows that do not depend on the routing go out first, every chunk's, straight into shared memory.
+  // A thread reads a shared row only after waiting for its own copies; the residual and gamma slices
+  // are read by any thread, after the barrier that follows every thread's wait.
   for (int ch = 0; ch < NCH; ++ch) {
     const int vec = vec0 + ch * SV;
     if (!in_group || vec >= nvec) break;
@@ -148,33 +154,33 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   cp_async_wait_all();
   __syncthreads();
 
-  // Group 0, chunk by chunk: rank sum in order 0..R-1, residual add (kept in place of the residual
-  // slice for the epilogue), sum of squares.
+  // The (chunk, vector) items of this CTA, spread over all its threads (item i to thread i mod the
+  // block; consecutive threads take consecutive vectors): rank sum in order 0..R-1, residual add (kept
+  // in place of the residual slice for the epilogue), sum of squares.
+  const int nitems = NCH * SV;
+  const int vbase = static_cast<int>(crank) * NCH * SV;  // the CTA's first vector
   float ss = 0.0f;
-  if (lead_group) {
-    for (int ch = 0; ch < NCH; ++ch) {
-      const int vec = vec0 + ch * SV;
-      if (vec >= nvec) break;
-      float S[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int rr = 0; rr < p.R; ++rr) {
-        float pr[8];
-        unpack8<A>(xch[(ch * p.R + rr) * SV + v], pr);
+  for (int it = tid; it < nitems; it += nthreads) {
+    const int ch = it / SV, vv = it - ch * SV;
+    if (vbase + it >= nvec) break;  // (vector vbase + it; later items are further along)
+    float S[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int rr = 0; rr < p.R; ++rr) {
+      float pr[8];
+      unpack8<A>(xch[(ch * p.R + rr) * SV + vv], pr);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) S[i] = __fadd_rn(S[i], pr[i]);
-      }
-      float res[8], x[8];
-      unpack8<A>(res_s[ch * SV + v], res);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[i] = Act<A>::round(__fadd_rn(Act<A>::round(S[i]), res[i]));
-        ss = __fmaf_rn(x[i], x[i], ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
-      }
-      const uint4 ro = make_uint4(Act<A>::pack(x[0], x[1]), Act<A>::pack(x[2], x[3]), Act<A>::pack(x[4], x[5]),
-                                  Act<A>::pack(x[6], x[7]));
-      res_s[ch * SV + v] = ro;
-      if (p.residual_out != nullptr)
-        *reinterpret_cast<uint4*>(p.residual_out + (static_cast<int64_t>(t) * H + vec * 8) * 2) = ro;
+      for (int i = 0; i < 8; ++i) S[i] = __fadd_rn(S[i], pr[i]);
     }
+    float res[8], x[8];
+    unpack8<A>(res_s[it], res);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[i] = Act<A>::round(__fadd_rn(Act<A>::round(S[i]), res[i]));
+      ss = __fmaf_rn(x[i], x[i], ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
+    }
+    // kept for the epilogue; written out with norm_out after the cluster barrier (whose release would
+    // otherwise wait for the global stores)
+    res_s[it] = make_uint4(Act<A>::pack(x[0], x[1]), Act<A>::pack(x[2], x[3]), Act<A>::pack(x[4], x[5]),
+                           Act<A>::pack(x[6], x[7]));
   }
 
   // Sum of squares: warp shuffle, warps in order, then the cluster's CTAs in rank order.
@@ -182,37 +188,50 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   const int warp = tid >> 5, lane = tid & 31;
   if (lane == 0) red[warp] = ss;
   __syncthreads();
-  if (tid == 0) {
+  if (C > 1) cluster_wait_acquire();  // all CTAs of the cluster have started (arrived on entry)
+  // Warp 0 reads the warp sums in parallel (lane i the i-th) and adds them in order with shuffles; with a
+  // cluster, lane c then writes the CTA's sum into slot `crank` of CTA c (C <= 16), so after one
+  // cluster barrier every CTA holds all the sums locally and adds them in rank order.
+  if (warp == 0) {
+    const int nw = nthreads >> 5;
+    const float mine = lane < nw ? red[lane] : 0.0f;
     float cta = 0.0f;
-    for (int w = 0; w < (nthreads >> 5); ++w) cta = __fadd_rn(cta, red[w]);
-    red[32] = cta;
+    for (int w = 0; w < nw; ++w) cta = __fadd_rn(cta, __shfl_sync(0xffffffffu, mine, w));
+    if (C > 1) {
+      if (lane < static_cast<int>(C)) dsmem_store_f32(&red[34 + crank], static_cast<uint32_t>(lane), cta);
+    } else if (lane == 0) {
+      red[33] = cta;
+    }
   }
   if (C > 1) {
+    // Every remote write is made before this barrier and none after it, so a CTA may exit as soon as
+    // it has passed the barrier.
     cluster_arrive_release();
     cluster_wait_acquire();
-    if (tid == 0) {
+    if (warp == 0) {
+      const float mine = lane < static_cast<int>(C) ? red[34 + lane] : 0.0f;
       float tot = 0.0f;
-      for (uint32_t c = 0; c < C; ++c) tot = __fadd_rn(tot, dsmem_load_f32(&red[32], c));
-      red[33] = tot;
+      for (uint32_t c = 0; c < C; ++c) tot = __fadd_rn(tot, __shfl_sync(0xffffffffu, mine, static_cast<int>(c)));
+      if (lane == 0) red[33] = tot;
     }
-    cluster_arrive_release();  // this CTA's remote reads are done; matched by the wait at the end
-  } else if (tid == 0) {
-    red[33] = red[32];
   }
   __syncthreads();
   const float rstd = rms_rstd(red[33], H, p.eps);
-  if (tid < ((SV + 31) & ~31)) {  // the warps that hold group 0 (whole warps, for the NVFP4 shuffles)
+  {
     const float qscale = (p.quant != MFR_QUANT_NONE) ? *p.quant_scale : 1.0f;
-    for (int ch = 0; ch < NCH; ++ch) {  // the same trip count for the whole warp
-      const int vec = vec0 + ch * SV;
-      const bool lead = lead_group && vec < nvec;
+    for (int base = 0; base < nitems; base += nthreads) {  // the same trip count for every thread (NVFP4 shuffles)
+      const int it = base + tid;
+      const bool act = it < nitems && vbase + it < nvec;
+      const int vec = vbase + it;
+      const uint4 ro = act ? res_s[it] : make_uint4(0, 0, 0, 0);
+      if (act && p.residual_out != nullptr)
+        *reinterpret_cast<uint4*>(p.residual_out + (static_cast<int64_t>(t) * H + vec * 8) * 2) = ro;
       float x[8], g[8];
-      unpack8<A>(lead ? res_s[ch * SV + v] : make_uint4(0, 0, 0, 0), x);
-      unpack8<A>(lead ? gam_s[ch * SV + v] : make_uint4(0, 0, 0, 0), g);
-      epilogue<A, 8>(p, t, vec * 8, lead, x, g, rstd, qscale);
+      unpack8<A>(ro, x);
+      unpack8<A>(act ? gam_s[it] : make_uint4(0, 0, 0, 0), g);
+      epilogue<A, 8>(p, t, vec * 8, act, x, g, rstd, qscale);
     }
   }
-  if (C > 1) cluster_wait_acquire();  // no CTA leaves while a peer may still read its shared memory
 }
 
 template <typename A, int KC>

@@ -174,6 +174,9 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -185,6 +188,14 @@ __device__ __forceinline__ float dsmem_load_f32(const float* local, uint32_t ran
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
   return v;
+}
+
+// Write a float into the shared memory of CTA `rank` of this cluster, at the address that `local` has
+// in this CTA (visible to that CTA after a cluster barrier with release/acquire semantics).
+__device__ __forceinline__ void dsmem_store_f32(float* local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void stg8(uint8_t* p, uint2 v) { *reinterpret_cast<uint2*>(p) = v; }

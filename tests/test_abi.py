@@ -147,6 +147,13 @@ def test_empty_batch_is_a_no_op(mfr):
     assert mfr.raw_library().moe_finalize_fused(ctypes.byref(a), None) == 0
 
 
+def test_gather_floor_rejects_bad_buffers(mfr):
+    lib = mfr.raw_library()
+    assert lib.moe_finalize_gather_floor_launch(None, None, 1, 512, None, None, 0) == -1
+    assert lib.moe_finalize_gather_floor_launch(0x1000, 0x1000, 1, 100, 0x1000, None, 0) == -1  # short rows
+    assert lib.moe_finalize_gather_floor_launch(0x1000, 0x1008, 1, 512, 0x1000, None, 0) == -1  # misaligned
+
+
 def test_status_strings(mfr):
     lib = mfr.raw_library()
     for s in (0, -1, -2, -3):

@@ -381,6 +381,20 @@ def test_kernel_choice_and_plan():
     assert p2["kernel"] == "stream" and p2["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count * 2
 
 
+def test_gather_floor_copies_the_indexed_row():
+    import moe_finalize_residual_gb300 as mfr
+    rows = torch.arange(64 * 256, dtype=torch.int32, device="cuda").view(64, 256)  # 1 KB rows
+    out = torch.zeros(128, dtype=torch.int32, device="cuda")
+    for i in (0, 37, 63):
+        mfr.moe_finalize_gather_floor_launch(torch.tensor([i], dtype=torch.int32, device="cuda"), rows, out)
+        torch.cuda.synchronize()
+        assert torch.equal(out, rows[i, :128])
+    before = out.clone()
+    mfr.moe_finalize_gather_floor_launch(torch.tensor([64], dtype=torch.int32, device="cuda"), rows, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, before)  # out of range: nothing written
+
+
 def test_deterministic_repeats():
     case = on_gpu(synth.make_case("det", T=33, H=4096, K=8, R=4, E=64, rsf=2.5, shared=True))
     for kernel in KERNELS:
