@@ -47,9 +47,10 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def algorithmic_bytes(case, quant="none") -> int:
+def algorithmic_bytes(case, quant="none", finalize_only=False) -> int:
     """Bytes the definition must move per call: routing, valid GEMM2 rows, shared rows, residual,
-    gamma, residual_out and the normalised (or quantised) output."""
+    gamma, residual_out and the normalised (or quantised) output; finalize-only: routing, rows, shared
+    rows and the finalized output."""
     T, H = case.T, case.H
     total = 0
     for r in range(case.R):
@@ -60,6 +61,8 @@ def algorithmic_bytes(case, quant="none") -> int:
         total += valid * H * 2
         if case.shared[r] is not None:
             total += T * H * 2
+    if finalize_only:
+        return total + T * H * 2
     total += T * H * 2 + H * 2 + T * H * 2
     total += {"none": T * H * 2, "fp8": T * H, "nvfp4": T * H // 2 + T * H // 16}[quant]
     return total
@@ -381,6 +384,57 @@ def main():
         extras["launch_floor_us"] = {"pdl": round(floor_pdl, 3), "no_pdl": round(floor_nopdl, 3),
                                      "gather_chain_pdl": round(floor_gather, 3)}
         del sets, outs, calls
+        torch.cuda.empty_cache()
+
+        # ---------------- finalize-only, and fused vs unfused (finalize, then residual + RMSNorm) ----
+        # L2-warm graphs of 20 launches, the pages' setting.  The unfused pair's second launch is this
+        # library's fused call on one partial whose route is masked and whose shared row is the first
+        # launch's output S, with factor 1: it reads S, the residual and gamma and writes residual_out
+        # and norm_out, the work of a separate residual-RMSNorm kernel; its outputs are checked equal
+        # to the fused call's.
+        fin = []
+        for (H, E, K, R, shared, T) in ((6144, 256, 8, 4, True, 1), (6144, 256, 8, 4, True, 16),
+                                        (6144, 256, 8, 4, True, 128), (2048, 512, 22, 1, False, 16),
+                                        (3584, 896, 16, 1, False, 16), (4096, 512, 32, 1, False, 16),
+                                        (4096, 512, 32, 1, False, 128)):
+            c = synth.make_case("fin", T=T, H=H, E=E, K=K, R=R, rsf=2.5, shared=shared, device=dev,
+                                scale_dtype=torch.float32 if R == 1 else torch.bfloat16, seed_base=500_000)
+            parts = [mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r]) for r in range(c.R)]
+            o = alloc_outs(mfr, c)[0]
+            s_out = torch.empty_like(c.residual)
+            masked = torch.full((T, 1), -1, dtype=torch.int32, device=dev)
+            second = [mfr.Partial(c.gemm2[0][:1], masked, None, s_out)]
+            ro2, no2 = torch.empty_like(c.residual), torch.empty_like(c.residual)
+
+            def fused(i):
+                mfr.moe_finalize_fused(parts, c.residual, c.gamma, routed_scaling_factor=c.rsf, eps=c.eps,
+                                       residual_out=o[0], norm_out=o[1], check=False)
+
+            def fin_only(i):
+                mfr.moe_finalize_routed(parts, routed_scaling_factor=c.rsf, out=s_out, check=False)
+
+            def unfused(i):
+                fin_only(i)
+                mfr.moe_finalize_fused(second, c.residual, c.gamma, routed_scaling_factor=1.0, eps=c.eps,
+                                       residual_out=ro2, norm_out=no2, check=False)
+            res = {}
+            for name, fn in (("fused_us", fused), ("finalize_only_us", fin_only), ("unfused_pair_us", unfused)):
+                gg = capture_graph(fn)
+                res[name], _ = time_graph(gg, 50, 5)
+                del gg
+            torch.cuda.synchronize()
+            def ordinal(x):  # 16-bit float bit patterns as an ordered integer line (+0 and -0 equal)
+                b = x.view(torch.int16).to(torch.int32)
+                return torch.where(b < 0, -(b & 0x7FFF), b)
+            same = bool(torch.equal(o[0], ro2))
+            norm_ulp = int((ordinal(o[1]) - ordinal(no2)).abs().max())
+            fb = algorithmic_bytes(c, finalize_only=True)
+            fin.append({"H": H, "K": K, "R": R, "T": T, **{k: round(v, 3) for k, v in res.items()},
+                        "finalize_only_gbs_l2_warm": round(fb / (res["finalize_only_us"] * 1e-6) / 1e9, 1),
+                        "unfused_over_fused": round(res["unfused_pair_us"] / res["fused_us"], 3),
+                        "unfused_residual_out_equal": same, "unfused_norm_out_max_ulp": norm_ulp})
+            del c, parts, o, s_out, second, ro2, no2
+        extras["finalize_only_and_unfused_l2_warm"] = fin
         torch.cuda.empty_cache()
 
         # ---------------- bandwidth regime: H7168, T16384, R4, top-8 (inputs >> L2) ----------------

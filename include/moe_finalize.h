@@ -54,7 +54,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define MFR_ABI_VERSION 1
+#define MFR_ABI_VERSION 2
 #define MFR_MAX_PARTIALS 8 /* R */
 #define MFR_MAX_TOP_K 64   /* K; the small-batch kernel of flashinfer PR #6546 takes 4 < topK <= 64 */
 #define MFR_MAX_HIDDEN 32768
@@ -136,6 +136,11 @@ typedef struct {
                                 bytes; padding bytes are not written.  Required iff NVFP4           */
   uint32_t flags;            /* MFR_FLAG_*                                                          */
   int32_t kernel;            /* mfr_kernel                                                          */
+  void* finalize_out;        /* device [T, H] act, or NULL: the finalized MoE output before the
+                                residual, S = round(sum over r of p_r) (p_0 when R = 1), the output
+                                of the standalone finalize (flashinfer PR #6546, Description:
+                                trtllm_moe_run_finalize; TensorRT-LLM PR #16778, Fix: the deferred
+                                finalize producer)                                                 */
 } mfr_args;
 
 /* Launch geometry chosen for a call (for tests and benchmarks). */
@@ -151,9 +156,11 @@ typedef struct {
 } mfr_plan;
 
 /* Enqueue the fused finalize.  Returns MFR_OK or a negative status (see above).
- * Required: partials[r].gemm2_out and perm_idx for every r, residual, gamma (also when norm_out is
- * NULL: the RMS is still needed for quantisation), and at least one of residual_out, norm_out,
- * quant_out.  Inputs and outputs must not overlap. */
+ * Required: partials[r].gemm2_out and perm_idx for every r, and at least one of residual_out,
+ * norm_out, quant_out, finalize_out.  residual and gamma are required unless finalize_out is the
+ * only output (finalize-only mode: no residual add, RMSNorm or quantisation is done and neither is
+ * read); gamma is needed also when norm_out is NULL, since the RMS feeds the quantisation.  Inputs
+ * and outputs must not overlap. */
 int moe_finalize_fused(const mfr_args* args, struct CUstream_st* stream);
 
 /* The geometry moe_finalize_fused would use for these arguments on the current device (validates

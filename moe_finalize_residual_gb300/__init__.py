@@ -24,7 +24,7 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "Partial", "moe_finalize_fused", "moe_finalize_plan", "moe_finalize_sf_bytes", "moe_finalize_quant_bytes",
+    "Partial", "moe_finalize_fused", "moe_finalize_routed", "moe_finalize_plan", "moe_finalize_sf_bytes", "moe_finalize_quant_bytes",
     "moe_finalize_empty_launch", "moe_finalize_gather_floor_launch", "moe_finalize_read_timeouts", "moe_finalize_abi_version", "library_path",
     "QUANT", "SF_LAYOUT", "KERNEL", "MFR_FLAG_PDL", "MFR_FLAG_ROUTING_READY",
 ]
@@ -55,7 +55,7 @@ class _CArgs(ctypes.Structure):
                 ("residual_out", ctypes.c_void_p), ("norm_out", ctypes.c_void_p),
                 ("quant_mode", ctypes.c_int32), ("sf_layout", ctypes.c_int32),
                 ("quant_scale", ctypes.c_void_p), ("quant_out", ctypes.c_void_p), ("sf_out", ctypes.c_void_p),
-                ("flags", ctypes.c_uint32), ("kernel", ctypes.c_int32)]
+                ("flags", ctypes.c_uint32), ("kernel", ctypes.c_int32), ("finalize_out", ctypes.c_void_p)]
 
 
 class _CPlan(ctypes.Structure):
@@ -134,18 +134,23 @@ def _as_device_scale(q, device) -> torch.Tensor:
 
 
 def _build_args(partials: Sequence[Partial], residual, gamma, routed_scaling_factor, eps, residual_out, norm_out,
-                quant_mode, quant_scale, sf_layout, quant_out, sf_out, flags, kernel, check=True):
+                quant_mode, quant_scale, sf_layout, quant_out, sf_out, flags, kernel, check=True, finalize_out=None):
     if len(partials) == 0:
         raise ValueError("at least one partial is required")
-    device = residual.device
-    T, H = residual.shape
-    K = partials[0].perm_idx.shape[1] if partials[0].perm_idx.dim() == 2 else 0
-    act = residual.dtype
+    p0 = partials[0]
+    device = residual.device if residual is not None else p0.gemm2_out.device
+    T = p0.perm_idx.shape[0] if p0.perm_idx.dim() == 2 else 0
+    H = residual.shape[1] if residual is not None else p0.gemm2_out.shape[1]
+    K = p0.perm_idx.shape[1] if p0.perm_idx.dim() == 2 else 0
+    act = residual.dtype if residual is not None else p0.gemm2_out.dtype
     sdt = None
     if check:
+        if residual is not None and residual.shape != (T, H):
+            raise ValueError(f"residual must be [{T}, {H}] (T from perm_idx)")
         # flashinfer PR #3385, review: every caller-provided tensor must be on the input's device.
         tensors = [("residual", residual), ("gamma", gamma), ("residual_out", residual_out), ("norm_out", norm_out),
-                   ("quant_out", quant_out), ("sf_out", sf_out), ("quant_scale", quant_scale)]
+                   ("quant_out", quant_out), ("sf_out", sf_out), ("quant_scale", quant_scale),
+                   ("finalize_out", finalize_out)]
         for r, p in enumerate(partials):
             tensors += [(f"partials[{r}].gemm2_out", p.gemm2_out), (f"partials[{r}].perm_idx", p.perm_idx),
                         (f"partials[{r}].expert_scale", p.expert_scale), (f"partials[{r}].shared_out", p.shared_out)]
@@ -158,7 +163,7 @@ def _build_args(partials: Sequence[Partial], residual, gamma, routed_scaling_fac
                 raise ValueError(f"{name} must be contiguous")
         if act not in (torch.bfloat16, torch.float16):
             raise ValueError(f"activation dtype {act} not supported (bfloat16 or float16)")
-        if gamma.shape != (H,) or gamma.dtype != act:
+        if gamma is not None and (gamma.shape != (H,) or gamma.dtype != act):
             raise ValueError("gamma must be [H] of the activation dtype")
         for r, p in enumerate(partials):
             if p.gemm2_out.dim() != 2 or p.gemm2_out.shape[1] != H or p.gemm2_out.dtype != act:
@@ -173,7 +178,7 @@ def _build_args(partials: Sequence[Partial], residual, gamma, routed_scaling_fac
                 sdt = p.expert_scale.dtype
             if p.shared_out is not None and (p.shared_out.shape != (T, H) or p.shared_out.dtype != act):
                 raise ValueError(f"partials[{r}].shared_out must be [{T}, {H}] {act}")
-        for name, t in (("residual_out", residual_out), ("norm_out", norm_out)):
+        for name, t in (("residual_out", residual_out), ("norm_out", norm_out), ("finalize_out", finalize_out)):
             if t is not None and (t.shape != (T, H) or t.dtype != act):
                 raise ValueError(f"{name} must be [{T}, {H}] {act}")
     else:
@@ -192,7 +197,8 @@ def _build_args(partials: Sequence[Partial], residual, gamma, routed_scaling_fac
     a.routed_scaling_factor = float(routed_scaling_factor)
     a.eps = float(eps)
     a.partials = ctypes.cast(parts, ctypes.POINTER(_CPartial))
-    a.residual, a.gamma = residual.data_ptr(), gamma.data_ptr()
+    a.residual, a.gamma = _ptr(residual), _ptr(gamma)
+    a.finalize_out = _ptr(finalize_out)
     a.residual_out, a.norm_out = _ptr(residual_out), _ptr(norm_out)
     a.quant_mode = QUANT[quant_mode] if isinstance(quant_mode, str) else int(quant_mode)
     a.sf_layout = SF_LAYOUT[sf_layout] if isinstance(sf_layout, str) else int(sf_layout)
@@ -209,12 +215,15 @@ def moe_finalize_fused(partials: Sequence[Partial], residual: torch.Tensor, gamm
                        quant_mode: str = "none", quant_scale=None, sf_layout: str = "row_major",
                        quant_out: Optional[torch.Tensor] = None, sf_out: Optional[torch.Tensor] = None,
                        pdl: bool = True, routing_ready: bool = False, kernel: str = "auto",
-                       stream: Optional[torch.cuda.Stream] = None, check: bool = True):
+                       stream: Optional[torch.cuda.Stream] = None, check: bool = True,
+                       finalize_out: Optional[torch.Tensor] = None):
     """Enqueue the fused finalize on ``stream`` (default: the current stream).
 
     Outputs that are not passed in are allocated (``want_*`` = False leaves them out).  Returns
     ``(residual_out, norm_out, quant_out, sf_out)`` with None for outputs not produced.
     ``quant_scale`` is the FP8 encode scale or the NVFP4 global scale (a float or a 1-element tensor).
+    ``finalize_out`` ([T, H] act), when given, also receives the finalized MoE output before the
+    residual (the rounded rank sum).
     """
     T, H = residual.shape
     dev = residual.device
@@ -237,11 +246,33 @@ def moe_finalize_fused(partials: Sequence[Partial], residual: torch.Tensor, gamm
         quant_scale = None
     flags = (MFR_FLAG_PDL if pdl else 0) | (MFR_FLAG_ROUTING_READY if routing_ready else 0)
     a, keep = _build_args(partials, residual, gamma, routed_scaling_factor, eps, residual_out, norm_out, qm,
-                          quant_scale, sf_layout, quant_out, sf_out, flags, kernel, check=check)
+                          quant_scale, sf_layout, quant_out, sf_out, flags, kernel, check=check,
+                          finalize_out=finalize_out)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     _check(_lib.moe_finalize_fused(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream)))
     del keep
     return residual_out, norm_out, quant_out, sf_out
+
+
+def moe_finalize_routed(partials: Sequence[Partial], *, routed_scaling_factor: float = 1.0,
+                        out: Optional[torch.Tensor] = None, pdl: bool = True, routing_ready: bool = False,
+                        kernel: str = "auto", stream: Optional[torch.cuda.Stream] = None,
+                        check: bool = True) -> torch.Tensor:
+    """Finalize-only mode: the finalized MoE output S = round(sum over r of p_r) ([T, H], the dtype of the
+    GEMM2 rows; p_0 when there is one partial), with no residual add, RMSNorm or quantisation -- the
+    standalone finalize that a deferred all-reduce or a separate residual-RMSNorm kernel consumes
+    (flashinfer PR #6546, Description; TensorRT-LLM PR #16778, Fix).  Returns ``out``."""
+    p0 = partials[0]
+    T, H = p0.perm_idx.shape[0], p0.gemm2_out.shape[1]
+    if out is None:
+        out = torch.empty(T, H, dtype=p0.gemm2_out.dtype, device=p0.gemm2_out.device)
+    flags = (MFR_FLAG_PDL if pdl else 0) | (MFR_FLAG_ROUTING_READY if routing_ready else 0)
+    a, keep = _build_args(partials, None, None, routed_scaling_factor, 1e-6, None, None, 0, None, "row_major", None,
+                          None, flags, kernel, check=check, finalize_out=out)
+    s = stream if stream is not None else torch.cuda.current_stream(out.device)
+    _check(_lib.moe_finalize_fused(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream)))
+    del keep
+    return out
 
 
 def moe_finalize_plan(partials: Sequence[Partial], residual: torch.Tensor, gamma: torch.Tensor, *,

@@ -103,9 +103,13 @@ int validate(const mfr_args* a) {
       return fail(MFR_ERR_INVALID_ARG, "partials[%d].expert_scale misaligned", r);
     if (!aligned(P.shared_out, 16)) return fail(MFR_ERR_INVALID_ARG, "partials[%d].shared_out not 16-byte aligned", r);
   }
-  if (a->residual == nullptr || a->gamma == nullptr) return fail(MFR_ERR_INVALID_ARG, "residual and gamma are required");
-  if (!aligned(a->residual, 16) || !aligned(a->gamma, 16) || !aligned(a->residual_out, 16) || !aligned(a->norm_out, 16))
-    return fail(MFR_ERR_INVALID_ARG, "residual, gamma, residual_out and norm_out must be 16-byte aligned");
+  const bool fin_only = a->finalize_out != nullptr && a->residual_out == nullptr && a->norm_out == nullptr &&
+                        a->quant_mode == MFR_QUANT_NONE;
+  if (!fin_only && (a->residual == nullptr || a->gamma == nullptr))
+    return fail(MFR_ERR_INVALID_ARG, "residual and gamma are required (unless finalize_out is the only output)");
+  if (!aligned(a->residual, 16) || !aligned(a->gamma, 16) || !aligned(a->residual_out, 16) ||
+      !aligned(a->norm_out, 16) || !aligned(a->finalize_out, 16))
+    return fail(MFR_ERR_INVALID_ARG, "residual, gamma, residual_out, norm_out and finalize_out must be 16-byte aligned");
   if (a->quant_mode != MFR_QUANT_NONE) {
     if (a->quant_out == nullptr || a->quant_scale == nullptr)
       return fail(MFR_ERR_INVALID_ARG, "quantisation needs quant_out and quant_scale");
@@ -114,7 +118,8 @@ int validate(const mfr_args* a) {
     if (!aligned(a->quant_scale, 4) || !aligned(a->quant_out, a->quant_mode == MFR_QUANT_FP8_E4M3 ? 4 : 2))
       return fail(MFR_ERR_INVALID_ARG, "quant_scale or quant_out misaligned");
   }
-  if (a->residual_out == nullptr && a->norm_out == nullptr && a->quant_mode == MFR_QUANT_NONE)
+  if (a->residual_out == nullptr && a->norm_out == nullptr && a->quant_mode == MFR_QUANT_NONE &&
+      a->finalize_out == nullptr)
     return fail(MFR_ERR_INVALID_ARG, "no output requested");
   return MFR_OK;
 }
@@ -141,6 +146,9 @@ void fill_params(const mfr_args* a, KParams* p) {
   p->gamma = static_cast<const uint8_t*>(a->gamma);
   p->residual_out = static_cast<uint8_t*>(a->residual_out);
   p->norm_out = static_cast<uint8_t*>(a->norm_out);
+  p->finalize_out = static_cast<uint8_t*>(a->finalize_out);
+  p->fin_only = (a->finalize_out != nullptr && a->residual_out == nullptr && a->norm_out == nullptr &&
+                 a->quant_mode == MFR_QUANT_NONE) ? 1 : 0;
   p->quant_out = static_cast<uint8_t*>(a->quant_out);
   p->sf_out = static_cast<uint8_t*>(a->sf_out);
   p->quant_scale = a->quant_scale;

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
 
   // Every CTA of the cluster arrives here on entry; the matching wait comes before the first write into
   // a peer's shared memory, so no CTA writes into one that has not started.
-  if (C > 1) cluster_arrive_relaxed();
+  if (C > 1 && !p.fin_only) cluster_arrive_relaxed();
   int2* rt = reinterpret_cast<int2*>(smem + p.off_routes) + (in_group ? r : 0) * p.K;  // this partial's routes
   if (p.pdl) pdl_launch_dependents();
   if (p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
     if (!in_group || vec >= nvec) break;
     const int64_t off = (static_cast<int64_t>(t) * H + vec * 8) * 2;
     if (has_shared) cp_async16(smem_addr(&xch[(ch * p.R + r) * SV + v]), P.shared + off);
-    if (lead_group) {
+    if (lead_group && !p.fin_only) {
       cp_async16(smem_addr(&res_s[ch * SV + v]), p.residual + off);
       cp_async16(smem_addr(&gam_s[ch * SV + v]), p.gamma + static_cast<int64_t>(vec) * 16);
     }
@@ -170,6 +170,11 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
 #pragma unroll
       for (int i = 0; i < 8; ++i) S[i] = __fadd_rn(S[i], pr[i]);
     }
+    if (p.finalize_out != nullptr)  // the finalized output S, rounded once
+      *reinterpret_cast<uint4*>(p.finalize_out + (static_cast<int64_t>(t) * H + (vbase + it) * 8) * 2) =
+          make_uint4(Act<A>::pack(S[0], S[1]), Act<A>::pack(S[2], S[3]), Act<A>::pack(S[4], S[5]),
+                     Act<A>::pack(S[6], S[7]));
+    if (p.fin_only) continue;
     float res[8], x[8];
     unpack8<A>(res_s[it], res);
 #pragma unroll
@@ -182,6 +187,8 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
     res_s[it] = make_uint4(Act<A>::pack(x[0], x[1]), Act<A>::pack(x[2], x[3]), Act<A>::pack(x[4], x[5]),
                            Act<A>::pack(x[6], x[7]));
   }
+
+  if (p.fin_only) return;  // finalize-only: no residual, RMSNorm or quantisation (the same for all threads)
 
   // Sum of squares: warp shuffle, warps in order, then the cluster's CTAs in rank order.
   ss = warp_sum(ss);

@@ -152,7 +152,7 @@ __device__ __forceinline__ int build_row_list(const KParams& p, int t, RowEntry*
   }
   if (lane == 0) {
     RowEntry res;
-    res.src = p.residual + static_cast<int64_t>(t) * p.H * 2;
+    res.src = p.fin_only ? nullptr : p.residual + static_cast<int64_t>(t) * p.H * 2;  // nothing to read
     res.scale = 1.0f;
     res.tag = kTagResidual;
     list[n] = res;
@@ -271,9 +271,11 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
         in_n = *reinterpret_cast<const int*>(e);
         ilist = reinterpret_cast<const RowEntry*>(e + 16);
       }
-      const uint8_t* src = ilist[ij].src + ipoff;
+      const uint8_t* row0 = ilist[ij].src;  // NULL: the closing entry of a finalize-only pass (no data)
+      const uint32_t m = row0 != nullptr ? imask : 0u;  // (no copy is made from the placeholder address)
+      const uint8_t* src = row0 != nullptr ? row0 + ipoff : reinterpret_cast<const uint8_t*>(p.part[0].perm);
 #pragma unroll
-      for (int q = 0; q < kQ; ++q) cp_async16_if(idst + q * QB, src + q * QB, (imask >> q) & 1u);
+      for (int q = 0; q < kQ; ++q) cp_async16_if(idst + q * QB, src + q * QB, (m >> q) & 1u);
       cp_async_commit();
       ++issued;
       idst += p.stage_bytes;
@@ -341,9 +343,21 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
       } else {  // the residual row closes the pass: residual_out = round(round(S) + residual)
         const int t = static_cast<int>(blockIdx.x) + ci * static_cast<int>(gridDim.x);
         const int64_t hoff = static_cast<int64_t>(cpass) * W + jt * 8;  // element of column 0
+        if (p.finalize_out != nullptr) {  // the finalized output S, rounded once
+#pragma unroll
+          for (int q = 0; q < kQ; ++q) {
+            if (cmask & (1u << q)) {
+              uint32_t w[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) w[c] = Act<A>::pack(S[4 * q + c].x, S[4 * q + c].y);
+              *reinterpret_cast<uint4*>(p.finalize_out + (static_cast<int64_t>(t) * H + hoff + q * NCT * 8) * 2) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
 #pragma unroll
         for (int q = 0; q < kQ; ++q) {
-          if (cmask & (1u << q)) {
+          if (!p.fin_only && (cmask & (1u << q))) {
             float2 res[4];
             unpack_pairs<A>(lds16(cdst + q * QB), res);
             uint32_t w[4];
@@ -376,6 +390,13 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
       cpass = pass_lo;
       cmask = colmask(cpass);
 
+      if (p.fin_only) {  // finalize-only: release the list; no RMSNorm
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rempty0 + 8u * (ci % kLists));
+        ci += tstride;
+        cn = -1;
+        continue;
+      }
       // Token done: release its list, reduce the sum of squares over the group's warps (all compute
       // warps in split mode), in warp order, double-buffered by token parity (the warps meet on an
       // mbarrier so the wait is bounded), and write norm_out and the quantised output from the kept

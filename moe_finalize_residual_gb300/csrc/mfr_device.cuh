@@ -41,6 +41,8 @@ struct KParams {
   const uint8_t* gamma;
   uint8_t* residual_out;
   uint8_t* norm_out;
+  uint8_t* finalize_out;  // the rounded rank sum S, or NULL
+  int32_t fin_only;       // finalize_out is the only output: no residual, RMSNorm or quantisation
   uint8_t* quant_out;
   uint8_t* sf_out;
   const float* quant_scale;

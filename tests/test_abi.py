@@ -57,7 +57,7 @@ int main(void) {
   F(mfr_args, routed_scaling_factor); F(mfr_args, eps); F(mfr_args, partials); F(mfr_args, residual);
   F(mfr_args, gamma); F(mfr_args, residual_out); F(mfr_args, norm_out); F(mfr_args, quant_mode);
   F(mfr_args, sf_layout); F(mfr_args, quant_scale); F(mfr_args, quant_out); F(mfr_args, sf_out);
-  F(mfr_args, flags); F(mfr_args, kernel);
+  F(mfr_args, flags); F(mfr_args, kernel); F(mfr_args, finalize_out);
   F(mfr_plan, kernel); F(mfr_plan, grid); F(mfr_plan, cluster); F(mfr_plan, block); F(mfr_plan, smem_bytes);
   F(mfr_plan, chunk); F(mfr_plan, stages);
   printf("MFR_MAX_PARTIALS %d\nMFR_MAX_TOP_K %d\nMFR_ABI_VERSION %d\n", MFR_MAX_PARTIALS, MFR_MAX_TOP_K, MFR_ABI_VERSION);
@@ -107,6 +107,8 @@ BAD = [
     dict(act_dtype=2), dict(scale_dtype=7), dict(quant_mode=3), dict(flags=8), dict(kernel=3),
     dict(residual=None), dict(gamma=None), dict(residual=0xB00008), dict(norm_out=0xE00004),
     dict(residual_out=None, norm_out=None),
+    dict(residual_out=None, norm_out=None, finalize_out=0xD00008),  # misaligned finalize_out
+    dict(residual=None, finalize_out=0xF30000),  # residual may be absent only when finalize_out is the only output
     dict(quant_mode=1), dict(quant_mode=2, quant_scale=0xF00000, quant_out=0xF10000),
     dict(quant_mode=2, quant_scale=0xF00000, quant_out=0xF10000, sf_out=0xF20000, sf_layout=2),
     dict(quant_mode=2, quant_scale=0xF00000, quant_out=0xF10000, sf_out=0xF20000, H=264),
@@ -140,6 +142,14 @@ def test_partial_pointer_checks(mfr):
     a, parts = _raw_args(mfr)
     parts[0].num_rows = -3
     assert lib.moe_finalize_fused(ctypes.byref(a), None) == -1
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU error path")
+def test_finalize_only_needs_no_residual_or_gamma(mfr):
+    """With finalize_out the only output, residual and gamma may be NULL: validation passes and the call
+    reaches the CUDA runtime (which reports no device here)."""
+    a, keep = _raw_args(mfr, residual=None, gamma=None, residual_out=None, norm_out=None, finalize_out=0xF30000)
+    assert mfr.raw_library().moe_finalize_fused(ctypes.byref(a), None) == -3
 
 
 def test_empty_batch_is_a_no_op(mfr):

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import synth
-from helpers import (CANARY, contraction_case, Guarded, as_f64, bits16, check_against_oracle, check_quant, partials_of,
+from helpers import (CANARY, contraction_case, Guarded, nan16, as_f64, bits16, check_against_oracle, check_quant, partials_of,
                      quant_scale_for, run, subcase, ulp_distance)
 
 pytestmark = pytest.mark.gpu
@@ -439,3 +439,64 @@ def _call_without_sf(mfr, parts, case, out):
 def test_no_wait_timed_out():
     import moe_finalize_residual_gb300 as mfr
     assert mfr.moe_finalize_read_timeouts() == 0
+
+
+# ------------------------------------------------------------------------------------------------------
+# Finalize-only mode: the rounded rank sum S (p_0 for one partial), no residual / RMSNorm / quant.
+
+FIN_CASES = {
+    "decode": dict(H=6144, K=8, R=4, E=64, rsf=2.5, shared=True),
+    "masked": dict(H=7168, K=10, R=2, E=64, act_dtype=torch.float16, scale_dtype=torch.float32,
+                   mask_quarter=True),
+    "highk": dict(H=4096, K=32, R=1, E=512, scale_dtype=torch.float32),
+    "single": dict(H=2048, K=6, R=1, E=32, rsf=2.5, shared=True),
+}
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("T", [1, 37, 300])
+@pytest.mark.parametrize("fam", sorted(FIN_CASES))
+def test_finalize_only(fam, T, kernel):
+    import moe_finalize_residual_gb300 as mfr
+    case = synth.make_case(f"fin-{fam}", T=T, device="cuda", **FIN_CASES[fam])
+    guard = Guarded(T * case.H * 2, "cuda", case.act_dtype, (T, case.H))
+    out = mfr.moe_finalize_routed(partials_of(case), routed_scaling_factor=case.rsf, out=guard.view,
+                                  kernel=kernel)
+    torch.cuda.synchronize()
+    assert guard.guards_intact(), "finalize_out guard overwritten"
+    toks = _sample_tokens(T) if T > 64 else np.arange(T)
+    sub = subcase(case, toks)
+    want = oracle.finalize(sub)["routed"]
+    got = bits16(out)[toks]
+    same = (got == want) | (nan16(got, case.act_dtype) & nan16(want, case.act_dtype))
+    assert same.all(), f"finalize_out: {np.count_nonzero(~same)} of {same.size} elements differ"
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_finalize_only_large_batch(kernel):
+    """Many tokens per CTA (both groups of the stream kernel, several chunks of the cluster kernel)."""
+    import moe_finalize_residual_gb300 as mfr
+    c = dict(synth.CONFIGS["bandwidth"])
+    c.pop("Ts")
+    case = synth.make_case("fin-bw", T=2048, H=7168, device="cuda", **c)
+    out = mfr.moe_finalize_routed(partials_of(case), routed_scaling_factor=case.rsf, kernel=kernel)
+    torch.cuda.synchronize()
+    toks = _sample_tokens(2048)
+    want = oracle.finalize(subcase(case, toks))["routed"]
+    assert np.array_equal(bits16(out)[toks], want)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_finalize_out_with_fused_outputs(kernel):
+    """finalize_out next to residual_out / norm_out: all three correct from one call."""
+    import moe_finalize_residual_gb300 as mfr
+    case = synth.make_case("fin-both", T=45, H=6144, K=8, R=4, E=64, rsf=2.5, shared=True, device="cuda")
+    fin = torch.empty_like(case.residual)
+    ro, no, _, _ = mfr.moe_finalize_fused(partials_of(case), case.residual, case.gamma,
+                                          routed_scaling_factor=case.rsf, eps=case.eps, kernel=kernel,
+                                          finalize_out=fin)
+    torch.cuda.synchronize()
+    want = oracle.finalize(case.to("cpu"))
+    assert np.array_equal(bits16(fin), want["routed"])
+    assert np.array_equal(bits16(ro), want["residual_out"])
+    assert ulp_distance(bits16(no), want["norm_out"], case.act_dtype).max() <= 1
