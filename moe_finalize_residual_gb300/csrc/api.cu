@@ -279,7 +279,6 @@ bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, La
       geo.grid = std::min(a->T, d.sms * bps);
       p->chunk = W;
       p->stages = kStreamSlots;
-      p->rdepth = kStreamLists;
       p->stage_bytes = slot_bytes;
       p->groups = G;
       p->split = split ? 1 : 0;
@@ -287,7 +286,6 @@ bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, La
       p->off_bar = 0;
       p->off_stage = off_stage;
       p->off_ring = off_ring;
-      p->off_gamma = 0;
       p->off_stash = off_stash;
       p->off_sred = off_sred;
       *g = geo;

@@ -94,7 +94,6 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   const int v = tid - r * SV;
   const int vec0 = static_cast<int>(crank) * NCH * SV + v;  // chunk ch holds vector vec0 + ch * SV
   const bool in_group = r < p.R;
-  const bool any = in_group && vec0 < nvec;     // the thread has a vector in chunk 0 (so it has work)
   uint4* xch = reinterpret_cast<uint4*>(smem);                // [NCH][R][SV] shared rows, then partial rows
   uint4* res_s = xch + NCH * p.R * SV;                        // [NCH][SV] residual slices, then residual_out
   uint4* gam_s = res_s + NCH * SV;                            // [NCH][SV] gamma slices

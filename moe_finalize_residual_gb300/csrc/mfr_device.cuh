@@ -63,12 +63,11 @@ struct KParams {
   // stream kernel
   int32_t chunk;          // hidden elements per pass
   int32_t stages;         // row buffers in the ring
-  int32_t rdepth;         // row-list ring depth (tokens)
   int32_t stage_bytes;    // bytes of one row buffer
   int32_t groups;         // stream kernel: groups of compute warps per CTA
   int32_t split;          // stream kernel: groups split each token's hidden passes (else the tokens)
   int32_t ring_bytes;     // bytes of one row-list entry
-  int32_t off_bar, off_stage, off_ring, off_gamma, off_stash, off_sred;
+  int32_t off_bar, off_stage, off_ring, off_stash, off_sred;
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -147,15 +146,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bulk (non-tensor) global -> shared copy completing on an mbarrier.  Addresses 16-byte aligned,
-// size a multiple of 16.  No multicast: the destination is this CTA's own shared memory.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -182,16 +172,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Read a float from the shared memory of CTA `rank` of this cluster at the address that `local`
-// has in this CTA.
-__device__ __forceinline__ float dsmem_load_f32(const float* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-
 // Write a float into the shared memory of CTA `rank` of this cluster, at the address that `local` has
 // in this CTA (visible to that CTA after a cluster barrier with release/acquire semantics).
 __device__ __forceinline__ void dsmem_store_f32(float* local, uint32_t rank, float v) {
@@ -199,8 +179,6 @@ __device__ __forceinline__ void dsmem_store_f32(float* local, uint32_t rank, flo
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
-
-__device__ __forceinline__ void stg8(uint8_t* p, uint2 v) { *reinterpret_cast<uint2*>(p) = v; }
 
 // Deterministic butterfly sum over the 32 lanes of a warp.
 __device__ __forceinline__ float warp_sum(float v) {
@@ -273,33 +251,11 @@ __device__ __forceinline__ void unpack8(uint4 raw, float v[8]) {
 
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
-// 16-byte load of data read once: through the non-coherent path, without allocating in L1.
-__device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ float load_scale(const void* base, int64_t i, int dtype) {
   if (base == nullptr) return 1.0f;  // absent expert scales read as 1.0
   if (dtype == MFR_FP32) return static_cast<const float*>(base)[i];
   const uint16_t b = static_cast<const uint16_t*>(base)[i];
   return dtype == MFR_BF16 ? __uint_as_float(static_cast<uint32_t>(b) << 16) : __half2float(__ushort_as_half(b));
-}
-
-// residual_out = round(round(S) + residual); returns the 4 values and adds their squares to ss.
-template <typename A>
-__device__ __forceinline__ uint2 residual_step(const float S[4], uint2 res_raw, float x[4], float& ss) {
-  float r[4];
-  unpack4<A>(res_raw, r);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[i] = Act<A>::round(__fadd_rn(Act<A>::round(S[i]), r[i]));
-    ss = __fmaf_rn(x[i], x[i], ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
-  }
-  return make_uint2(Act<A>::pack(x[0], x[1]), Act<A>::pack(x[2], x[3]));
 }
 
 // rstd = 1 / sqrt(sum/H + eps), each operation correctly rounded.
@@ -376,15 +332,6 @@ __device__ __forceinline__ void epilogue(const KParams& p, int64_t t, int h, boo
       if ((h & 15) == 0) p.sf_out[sf_offset(t, h >> 4, p.H, p.sf_layout)] = sf;
     }
   }
-}
-
-// The 4-element form used by the stream kernel: gamma arrives as 4 packed act values.
-template <typename A>
-__device__ __forceinline__ void epilogue4(const KParams& p, int64_t t, int h, bool active, const float x[4],
-                                          uint2 gamma_raw, float rstd, float qscale) {
-  float g[4];
-  unpack4<A>(gamma_raw, g);
-  epilogue<A, 4>(p, t, h, active, x, g, rstd, qscale);
 }
 
 }  // namespace mfr
