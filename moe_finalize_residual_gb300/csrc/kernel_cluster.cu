@@ -48,7 +48,7 @@ __device__ __forceinline__ void fill_routes(const KParams& p, const KPartial& P,
 // read again for its FMA, so the indices and scales need no registers while the loads are in flight.
 template <typename A, int KC>
 __device__ __forceinline__ void gather_chain(const KPartial& P, int H, int K, int vec, const int2* rt, int k0,
-                                             float acc[8]) {
+                                             float2 acc[4]) {
   uint4 d[KC];
 #pragma unroll
   for (int j = 0; j < KC; ++j) {
@@ -61,12 +61,12 @@ __device__ __forceinline__ void gather_chain(const KPartial& P, int H, int K, in
     if (k0 + j < K) {
       int ix, scb;
       asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(ix), "=r"(scb) : "r"(rt_s + 8u * j) : "memory");
-      if (ix >= 0) {
-        float x[8];
-        unpack8<A>(d[j], x);
-        const float sc = __int_as_float(scb);
+      if (ix >= 0) {  // element pairs by the packed FMA, each lane rounded like fmaf
+        float2 x[4];
+        unpack_pairs<A>(d[j], x);
+        const float2 sc = make_float2(__int_as_float(scb), __int_as_float(scb));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(sc, x[i], acc[i]);
+        for (int i = 0; i < 4; ++i) acc[i] = __ffma2_rn(sc, x[i], acc[i]);
       }
     }
   }
@@ -133,18 +133,20 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   for (int ch = 0; ch < NCH; ++ch) {
     const int vec = vec0 + ch * SV;
     if (!in_group || vec >= nvec) break;
-    float acc[8];
+    float2 acc[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
     for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain<A, KC>(P, H, p.K, vec, rt, k0, acc);
     if (ch == 0) cp_async_wait_all();
     uint4* xr = &xch[(ch * p.R + r) * SV + v];
     float shv[8];
     unpack8<A>(*xr, shv);
+    // Scalar operations here: a packed multiply followed by a packed add of its result may be
+    // contracted into one packed FMA, which rounds once instead of twice.
     float a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      a[i] = __fmul_rn(acc[i], p.rsf);
+      a[i] = __fmul_rn((i & 1) ? acc[i >> 1].y : acc[i >> 1].x, p.rsf);
       if (has_shared) a[i] = __fadd_rn(a[i], shv[i]);
     }
     *xr = make_uint4(Act<A>::pack(a[0], a[1]), Act<A>::pack(a[2], a[3]), Act<A>::pack(a[4], a[5]),
@@ -162,29 +164,33 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   for (int it = tid; it < nitems; it += nthreads) {
     const int ch = it / SV, vv = it - ch * SV;
     if (vbase + it >= nvec) break;  // (vector vbase + it; later items are further along)
-    float S[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int rr = 0; rr < p.R; ++rr) {
-      float pr[8];
-      unpack8<A>(xch[(ch * p.R + rr) * SV + vv], pr);
+    float2 S[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) S[i] = __fadd_rn(S[i], pr[i]);
+    for (int i = 0; i < 4; ++i) S[i] = make_float2(0.0f, 0.0f);
+    for (int rr = 0; rr < p.R; ++rr) {
+      float2 pr[4];
+      unpack_pairs<A>(xch[(ch * p.R + rr) * SV + vv], pr);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) S[i] = __fadd2_rn(S[i], pr[i]);
     }
     if (p.finalize_out != nullptr)  // the finalized output S, rounded once
       *reinterpret_cast<uint4*>(p.finalize_out + (static_cast<int64_t>(t) * H + (vbase + it) * 8) * 2) =
-          make_uint4(Act<A>::pack(S[0], S[1]), Act<A>::pack(S[2], S[3]), Act<A>::pack(S[4], S[5]),
-                     Act<A>::pack(S[6], S[7]));
+          make_uint4(Act<A>::pack(S[0].x, S[0].y), Act<A>::pack(S[1].x, S[1].y), Act<A>::pack(S[2].x, S[2].y),
+                     Act<A>::pack(S[3].x, S[3].y));
     if (p.fin_only) continue;
-    float res[8], x[8];
-    unpack8<A>(res_s[it], res);
+    float2 res[4];
+    unpack_pairs<A>(res_s[it], res);
+    uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[i] = Act<A>::round(__fadd_rn(Act<A>::round(S[i]), res[i]));
-      ss = __fmaf_rn(x[i], x[i], ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = round_pair<A>(__fadd2_rn(round_pair<A>(S[i]), res[i]));
+      ss = __fmaf_rn(x.x, x.x, ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
+      ss = __fmaf_rn(x.y, x.y, ss);
+      w[i] = Act<A>::pack(x.x, x.y);
     }
     // kept for the epilogue; written out with norm_out after the cluster barrier (whose release would
     // otherwise wait for the global stores)
-    res_s[it] = make_uint4(Act<A>::pack(x[0], x[1]), Act<A>::pack(x[2], x[3]), Act<A>::pack(x[4], x[5]),
-                           Act<A>::pack(x[6], x[7]));
+    res_s[it] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 
   if (p.fin_only) return;  // finalize-only: no residual, RMSNorm or quantisation (the same for all threads)
