@@ -168,6 +168,31 @@ def finalize(case, t0: int = 0, t1: int | None = None, mode: int = MODE_FP32_ACC
     return out
 
 
+def finalize_threads(case, threads: int, t0: int = 0, t1: int | None = None, mode: int = MODE_FP32_ACCUM):
+    """``finalize`` with tokens [t0, t1) split into ``threads`` contiguous ranges, each run by its own host
+    thread (ctypes releases the GIL during the C call).  Tokens are independent and each is computed by
+    the same code in the same order, so the result is bit-identical to ``finalize``."""
+    t1 = case.T if t1 is None else t1
+    out = {k: np.zeros((case.T, case.H), dtype=np.uint16) for k in ("residual_out", "norm_out", "routed")}
+    n = max(1, min(int(threads), t1 - t0))
+    bounds = [t0 + (t1 - t0) * i // n for i in range(n + 1)]
+    keep, blocks = [], []
+    for i in range(n):
+        a = _args(case, bounds[i], bounds[i + 1], mode, keep)
+        a.residual_out = out["residual_out"].ctypes.data
+        a.norm_out = out["norm_out"].ctypes.data
+        a.routed_out = out["routed"].ctypes.data
+        blocks.append(a)
+    L = lib()
+    workers = [threading.Thread(target=L.oracle_finalize, args=(ctypes.byref(a),)) for a in blocks[1:]]
+    for w in workers:
+        w.start()
+    L.oracle_finalize(ctypes.byref(blocks[0]))
+    for w in workers:
+        w.join()
+    return out
+
+
 def finalize_fp64(case, t0: int = 0, t1: int | None = None):
     """FP64 evaluation of the same formula without intermediate rounding: (residual_ref, norm_ref)."""
     t1 = case.T if t1 is None else t1

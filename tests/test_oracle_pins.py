@@ -549,3 +549,18 @@ def test_mutant_is_caught(mutant, tmp_path):
     with oracle.use_library(path):
         failed = all_pins()
     assert failed, f"no pin caught the mutant '{mutant}'"
+
+
+@pytest.mark.parametrize("threads", [1, 3, 16])
+def test_threaded_oracle_is_bit_identical(threads):
+    # The host-core baseline runs the oracle over token ranges in parallel; every token must come out
+    # exactly as the single-threaded run gives it (masked routes, fp16, more threads than tokens).
+    c = synth.make_case("thr", T=7, H=256, K=6, R=2, E=16, act_dtype=torch.float16, mask_quarter=True,
+                        scale_dtype=torch.float32)
+    a = oracle.finalize(c)
+    b = oracle.finalize_threads(c, threads)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    part = oracle.finalize_threads(c, threads, 2, 5)
+    assert np.array_equal(part["norm_out"][2:5], a["norm_out"][2:5])
+    assert not part["norm_out"][:2].any() and not part["norm_out"][5:].any()
