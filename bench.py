@@ -374,6 +374,16 @@ def main():
 
     extras = {}
     if rank == 0 and not args.no_extras:
+        # ---------------- the headline again with the early routing read (MFR_FLAG_ROUTING_READY) ----------
+        # Safe here and in a MoE layer: the routing is written long before the GEMM that precedes the
+        # finalize, and back-to-back finalize launches do not write it.  Same rotating input sets.
+        calls_rr = [finalize_fn(mfr, c, o, routing_ready=True) for c, o in zip(sets, outs)]
+        grr = capture_graph(lambda i: calls_rr[i % nsets]())
+        rr_us, _ = time_graph(grr, 200, 20)
+        extras["headline_routing_ready"] = {"us": round(rr_us, 3),
+                                            "gbs": round(bytes_call / (rr_us * 1e-6) / 1e9, 1),
+                                            "frac": round(bytes_call / (rr_us * 1e-6) / 1e9 / peak, 4)}
+        del grr, calls_rr
         # ---------------- token sweep, L2-warm (the pages' setting), and launch floors -------------
         sweep = []
         for T in (1, 4, 16, 32, 64, 128):
