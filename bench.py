@@ -468,6 +468,32 @@ def main():
         extras["finalize_only_and_unfused_l2_warm"] = fin
         torch.cuda.empty_cache()
 
+        # ---------------- every case of the tiny, masked and high-top-k workloads (L2-warm, like the
+        # pages' latency tables) and the bandwidth workload's H x T grid (inputs larger than L2) ----------
+        t_cfg = time.perf_counter()
+        rows_cfg = []
+        for fam in ("tiny", "masked", "highk", "bandwidth"):
+            for c in synth.config_cases(fam, device=dev):
+                o = alloc_outs(mfr, c)[0]
+                fn = finalize_fn(mfr, c, o)
+                big = fam == "bandwidth"
+                gg = capture_graph(lambda i: fn(), n=4 if big else GRAPH_LAUNCHES)
+                us, _ = time_graph(gg, 5 if big else 30, 2 if big else 3, launches=4 if big else GRAPH_LAUNCHES)
+                p = mfr.moe_finalize_plan([mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r])
+                                           for r in range(c.R)], c.residual, c.gamma)
+                b = algorithmic_bytes(c)
+                row = {"family": fam, "T": c.T, "H": c.H, "K": c.K, "R": c.R,
+                       "act": str(c.act_dtype).replace("torch.", ""),
+                       "scale": str(c.scale_dtype).replace("torch.", ""), "kernel": p["kernel"], "us": round(us, 3),
+                       "gbs": round(b / (us * 1e-6) / 1e9, 1), "l2": "inputs > L2" if big else "warm"}
+                if big:
+                    row["frac"] = round(b / (us * 1e-6) / 1e9 / peak, 3)
+                rows_cfg.append(row)
+                del gg, o, c
+            torch.cuda.empty_cache()
+        extras["configs"] = rows_cfg
+        extras["configs_wall_s"] = round(time.perf_counter() - t_cfg, 1)
+
         # ---------------- bandwidth regime: H7168, T16384, R4, top-8 (inputs >> L2) ----------------
         bw = []
         c = synth.make_case("bandwidth-H7168-T16384", T=16384, H=7168, device=dev,

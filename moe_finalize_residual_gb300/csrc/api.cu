@@ -185,7 +185,10 @@ constexpr int kMaxCluster = MFR_CLUSTER_MAX_SIZE;
 // for all R partials (R*SV threads).  C comes from the parallelism target (about two CTAs per SM over
 // the batch), SV is capped by the preferred CTA size, and NCH covers the rest of the row; C <= 16 and
 // R*SV <= kClusterMaxThreads.
-bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
+// This plans one form of the kernel (kc routes in flight per thread) and reports how many waves of
+// resident clusters its grid takes.
+bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, KParams* p, LaunchGeom* g,
+                       int64_t* waves_out) {
   const int nvec = a->H / 8;
   const int unit = (a->H % 16 == 0) ? 2 : 1;  // slices start on 16-element blocks when H allows
   const int R = a->R;
@@ -197,11 +200,23 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
   // Cluster sizes of 5-7 and 9-15 CTAs measured slower than the next smaller size in {1, 2, 3, 4, 8, 16}.
   const int c_raw = std::max(1, std::min(kMaxCluster, (MFR_CLUSTER_CTAS_PER_SM * d.sms) / std::max(1, a->T)));
   const int c_goal = c_raw >= 16 ? 16 : c_raw >= 8 ? 8 : c_raw >= 4 ? 4 : c_raw;
-  for (int cg = c_goal; cg <= kMaxCluster; ++cg) {
+  // Candidates in order of preference: c_goal, larger counts (when shared memory is short), then smaller
+  // ones.  The first whose grid runs in one wave of resident clusters wins, else the one with the fewest
+  // waves.  (The 16-routes-in-flight form takes about 120 registers a thread, so only one 448- or
+  // 512-thread CTA fits on an SM, and c_goal's grid would take two waves.)
+  int cands[kMaxCluster + 8];
+  int ncand = 0;
+  for (int cg = c_goal; cg <= kMaxCluster; ++cg) cands[ncand++] = cg;
+  for (int cg : {8, 4, 3, 2, 1})
+    if (cg < c_goal) cands[ncand++] = cg;
+  bool found = false;
+  int64_t best_waves = 0;
+  for (int i = 0; i < ncand; ++i) {
+    const int cg = cands[i];
     const int sv = std::min(sv_soft, align_up(ceil_div(nvec, cg), unit));
     const int nch = ceil_div(nvec, cg * sv);
     const int C = ceil_div(nvec, nch * sv);
-    if (C > kMaxCluster) return false;
+    if (C > kMaxCluster) continue;
     const int sv_fit = align_up(ceil_div(nvec, C * nch), unit);  // even slices
     const int block = align_up(sv_fit * R, 32);
     const int off_red = align_up((R + 2) * nch * sv_fit * 16, 16);
@@ -209,29 +224,56 @@ bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, L
     const int smem = align_up(off_routes + R * a->K * 8, 16);
     if (smem > d.smem_optin) continue;
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
-    if (C > 1) {
-      const auto key = std::make_tuple(dev, a->act_dtype * 2 + (a->K > 8 ? 1 : 0), C, block, smem);
-      int n;
-      {
-        std::lock_guard<std::mutex> lock(g_mu);
-        auto it = g_cluster_ok.find(key);
-        n = (it == g_cluster_ok.end()) ? -1 : it->second;
-      }
-      if (n < 0) {
-        n = cluster_kernel_max_active_clusters(a->act_dtype, a->K, geo);
-        std::lock_guard<std::mutex> lock(g_mu);
-        g_cluster_ok[key] = n;
-      }
-      if (n < 1) continue;
+    // clusters (of C CTAs; single CTAs when C = 1) the GPU holds at once
+    const auto key = std::make_tuple(dev, a->act_dtype * 2 + (kc == 8 ? 0 : 1), C, block, smem);
+    int n;
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      auto it = g_cluster_ok.find(key);
+      n = (it == g_cluster_ok.end()) ? -1 : it->second;
     }
+    if (n < 0) {
+      n = C > 1 ? cluster_kernel_max_active_clusters(a->act_dtype, kc, geo)
+                : d.sms * cluster_kernel_blocks_per_sm(a->act_dtype, kc, geo);
+      std::lock_guard<std::mutex> lock(g_mu);
+      g_cluster_ok[key] = n;
+    }
+    if (n < 1) continue;
+    const int64_t waves = (static_cast<int64_t>(a->T) + n - 1) / n;
+    if (found && waves >= best_waves) continue;
+    found = true;
+    best_waves = waves;
     p->slice_vec = sv_fit;
     p->nchunk = nch;
+    p->route_batch = kc;
     p->off_red = off_red;
     p->off_routes = off_routes;
     *g = geo;
+    *waves_out = waves;
+    if (waves == 1) break;
+  }
+  return found;
+}
+
+// Top-k up to 8: eight routes in flight per thread.  Top-k 9..16: sixteen in flight (one round), unless
+// that form's plan holds only one CTA per SM (a block of 384 or more threads at about 120 registers a
+// thread) or takes more than one wave; then eight in flight over two rounds, with two CTAs per SM,
+// measured faster (top-10, R=4, H=7168: T=128 14.2 against 15.6 µs, T=16 6.1 against 6.3; top-16,
+// R=4, T=64: 10.6 against 12.9), while small blocks keep the single round (top-16, R=1, H=3584,
+// T=128: 5.4 against 7.3).  Larger top-k: sixteen in flight.
+bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
+  int64_t waves = 0;
+  if (a->K <= 8) return plan_cluster_form(a, d, dev, 8, p, g, &waves);
+  const bool ok16 = plan_cluster_form(a, d, dev, 16, p, g, &waves);
+  if (a->K > 16 || (ok16 && g->block < 384 && waves == 1)) return ok16;
+  KParams p8 = *p;
+  LaunchGeom g8{};
+  if (plan_cluster_form(a, d, dev, 8, &p8, &g8, &waves)) {
+    *p = p8;
+    *g = g8;
     return true;
   }
-  return false;
+  return ok16;
 }
 
 // Stream kernel: persistent CTAs (one per SM) of a routing warp and kStreamGroups groups of compute

@@ -305,17 +305,35 @@ static int max_active_clusters(const LaunchGeom& g) {
   return n;
 }
 
-// Routes in flight per thread: 8 covers top-k <= 8 in one round; larger top-k go 16 at a time.
-cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  if (act_dtype == MFR_BF16)
-    return p.K <= 8 ? launch_cluster<__nv_bfloat16, 8>(p, g, stream) : launch_cluster<__nv_bfloat16, 16>(p, g, stream);
-  return p.K <= 8 ? launch_cluster<__half, 8>(p, g, stream) : launch_cluster<__half, 16>(p, g, stream);
+template <typename A, int KC>
+static int blocks_per_sm(const LaunchGeom& g) {
+  auto kern = cluster_finalize_kernel<A, KC>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, g.block, g.smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
-int cluster_kernel_max_active_clusters(int act_dtype, int K, const LaunchGeom& g) {
+// Routes in flight per thread (the plan's route_batch): 8, or 16 for larger top-k when that fits better.
+cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
   if (act_dtype == MFR_BF16)
-    return K <= 8 ? max_active_clusters<__nv_bfloat16, 8>(g) : max_active_clusters<__nv_bfloat16, 16>(g);
-  return K <= 8 ? max_active_clusters<__half, 8>(g) : max_active_clusters<__half, 16>(g);
+    return p.route_batch == 8 ? launch_cluster<__nv_bfloat16, 8>(p, g, stream)
+                              : launch_cluster<__nv_bfloat16, 16>(p, g, stream);
+  return p.route_batch == 8 ? launch_cluster<__half, 8>(p, g, stream) : launch_cluster<__half, 16>(p, g, stream);
+}
+
+int cluster_kernel_blocks_per_sm(int act_dtype, int kc, const LaunchGeom& g) {
+  if (act_dtype == MFR_BF16) return kc == 8 ? blocks_per_sm<__nv_bfloat16, 8>(g) : blocks_per_sm<__nv_bfloat16, 16>(g);
+  return kc == 8 ? blocks_per_sm<__half, 8>(g) : blocks_per_sm<__half, 16>(g);
+}
+
+int cluster_kernel_max_active_clusters(int act_dtype, int kc, const LaunchGeom& g) {
+  if (act_dtype == MFR_BF16)
+    return kc == 8 ? max_active_clusters<__nv_bfloat16, 8>(g) : max_active_clusters<__nv_bfloat16, 16>(g);
+  return kc == 8 ? max_active_clusters<__half, 8>(g) : max_active_clusters<__half, 16>(g);
 }
 
 }  // namespace mfr

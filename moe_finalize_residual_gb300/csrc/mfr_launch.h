@@ -31,6 +31,7 @@ static_assert(kStreamLists % kStreamGroups == 0, "a list slot must return to the
 static_assert(kStreamGroups == 1 || kStreamGroups == 2, "the stream kernel is built for one or two groups");
 constexpr int kClusterMaxThreads = 512;             // R groups of SV threads
 
+
 struct LaunchGeom {
   int grid;
   int block;
@@ -40,7 +41,9 @@ struct LaunchGeom {
 };
 
 cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
-int cluster_kernel_max_active_clusters(int act_dtype, int K, const LaunchGeom& g);
+// kc: routes in flight per thread, 8 (two 512-thread CTAs fit on an SM) or 16 (one)
+int cluster_kernel_max_active_clusters(int act_dtype, int kc, const LaunchGeom& g);
+int cluster_kernel_blocks_per_sm(int act_dtype, int kc, const LaunchGeom& g);
 cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
 int stream_kernel_blocks_per_sm(int act_dtype, int groups, const LaunchGeom& g);
 cudaError_t read_and_reset_timeouts(unsigned int* count);
