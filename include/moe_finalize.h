@@ -195,10 +195,11 @@ int moe_finalize_empty_launch(struct CUstream_st* stream, uint32_t flags);
 int moe_finalize_gather_floor_launch(const int32_t* idx, const void* rows, int64_t nrows, int64_t row_bytes,
                                      void* out, struct CUstream_st* stream, uint32_t flags);
 
-/* Robustness aid (no counterpart on the pages): the stream kernel bounds every wait on its own
- * pipeline barriers (about 2 s); a wait that runs out records a count on the device and the kernel
- * returns early.  This reads the count for the current device into *count and resets it.  It
- * synchronizes the device.  A nonzero count means the outputs of some call are incomplete. */
+/* Robustness aid (no counterpart on the pages): every wait in the kernels is bounded (about 2 s): the
+ * stream kernel's waits on its pipeline barriers and the cluster kernel's wait for its peers' sums of
+ * squares.  A wait that runs out records a count on the device and the kernel goes on or returns
+ * early.  This reads the count for the current device into *count and resets it.  It synchronizes
+ * the device.  A nonzero count means the outputs of some call are incomplete or wrong. */
 int moe_finalize_read_timeouts(uint32_t* count);
 
 /* MFR_ABI_VERSION of the loaded library. */

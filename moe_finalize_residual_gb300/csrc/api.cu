@@ -220,7 +220,7 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     const int sv_fit = align_up(ceil_div(nvec, C * nch), unit);  // even slices
     const int block = align_up(sv_fit * R, 32);
     const int off_red = align_up((R + 2) * nch * sv_fit * 16, 16);
-    const int off_routes = align_up(off_red + 50 * 4, 16);
+    const int off_routes = align_up(off_red + 56 * 4, 16);  // 50 floats, then the exchange mbarrier
     const int smem = align_up(off_routes + R * a->K * 8, 16);
     if (smem > d.smem_optin) continue;
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
@@ -495,10 +495,11 @@ int moe_finalize_gather_floor_launch(const int32_t* idx, const void* rows, int64
 
 int moe_finalize_read_timeouts(uint32_t* count) {
   if (count == nullptr) return fail(MFR_ERR_INVALID_ARG, "count is NULL");
-  unsigned int c = 0;
+  unsigned int c = 0, cc = 0;
   cudaError_t e = read_and_reset_timeouts(&c);
-  if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "reading the timeout counter: %s", cudaGetErrorString(e));
-  *count = c;
+  if (e == cudaSuccess) e = read_and_reset_cluster_timeouts(&cc);
+  if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "reading the timeout counters: %s", cudaGetErrorString(e));
+  *count = c + cc;
   return MFR_OK;
 }
 

@@ -16,15 +16,16 @@
 //    every partial row is produced by one thread in the definition's order, so it is bit-exact;
 //  * the shared-expert, residual and gamma slices of every chunk are copied into shared memory first;
 //    each group writes its rounded partial rows to shared memory (one buffer per chunk, so one barrier
-//    serves all chunks); group 0 sums the R rows in rank order (the shared-memory combine), adds the
-//    residual and writes residual_out, keeping it in shared memory for the epilogue;
+//    serves all chunks); the (chunk, vector) items are then spread over all threads for the rank sum
+//    in order (the shared-memory combine) and the residual add, residual_out kept in shared memory;
 //  * the sum of squares is reduced with warp shuffles, then across warps in shared memory, then across
-//    the cluster's CTAs: each CTA writes its sum into a slot of every peer's shared memory, and after
-//    one cluster barrier every CTA adds the slots in rank order, so all get the same deterministic
-//    total; group 0 then writes residual_out, norm_out and the quantised output.
+//    the cluster's CTAs: each CTA sends its sum into a slot of every peer's shared memory with st.async,
+//    counted on the peer's mbarrier, and once its own mbarrier has all C sums every CTA adds the slots
+//    in rank order, so all get the same deterministic total; then all threads write residual_out,
+//    norm_out and the quantised output.
 //
-// No CTA waits on a flag in global memory; the only cross-CTA synchronisation is the hardware cluster
-// barrier, which every CTA reaches unconditionally.
+// No CTA waits on a flag in global memory.  Across CTAs there is the hardware cluster barrier at entry
+// (every CTA reaches it unconditionally) and the exchange's mbarrier, whose wait is bounded.
 #include "mfr_device.cuh"
 #include "mfr_launch.h"
 
@@ -72,6 +73,23 @@ __device__ __forceinline__ void gather_chain(const KPartial& P, int H, int K, in
   }
 }
 
+// Waits on the cluster exchange's mbarrier (phase 0) that end early: a wait is bounded at about 2 s of
+// device time; one that runs out is counted here and the CTA goes on (its outputs are then wrong, which
+// the count reports: moe_finalize_read_timeouts).
+__device__ unsigned int g_cluster_wait_timeouts = 0;
+
+__device__ __forceinline__ void cluster_exchange_wait(uint32_t bar) {
+  if (mbar_try_wait(bar, 0)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, 0)) return;
+    if ((it & 31u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+      if ((threadIdx.x & 31) == 0) atomicAdd(&g_cluster_wait_timeouts, 1u);
+      return;
+    }
+  }
+}
+
 // Resident CTAs the compiler must allow for (it sets the register budget): two 512-thread CTAs per SM
 // for the 8-routes-in-flight form.
 #ifndef MFR_CLUSTER_MIN_BLOCKS
@@ -98,13 +116,22 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   uint4* res_s = xch + NCH * p.R * SV;                        // [NCH][SV] residual slices, then residual_out
   uint4* gam_s = res_s + NCH * SV;                            // [NCH][SV] gamma slices
   float* red = reinterpret_cast<float*>(smem + p.off_red);    // [0,32) warp sums, [32] CTA sum, [33] total,
-                                                              // [34,50) the cluster's CTA sums by rank
+                                                              // [34,50) the cluster's CTA sums by rank,
+                                                              // [52,54) the exchange's mbarrier
   const KPartial& P = p.part[in_group ? r : 0];
   const bool has_shared = in_group && ((p.shared_mask >> r) & 1u);
   const bool lead_group = r == 0;               // group 0 finishes the token
 
   // Every CTA of the cluster arrives here on entry; the matching wait comes before the first write into
   // a peer's shared memory, so no CTA writes into one that has not started.
+  // The cluster exchange's mbarrier: it completes once all C CTAs' sums (4 bytes each) have landed here.
+  // It is set up before the entry arrive, so a peer that has passed the matching wait may write to it.
+  const uint32_t xbar = smem_addr(red + 52);
+  if (C > 1 && !p.fin_only && tid == 0) {
+    mbar_init(xbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(xbar, 4u * C);
+  }
   if (C > 1 && !p.fin_only) cluster_arrive_relaxed();
   int2* rt = reinterpret_cast<int2*>(smem + p.off_routes) + (in_group ? r : 0) * p.K;  // this partial's routes
   if (p.pdl) pdl_launch_dependents();
@@ -188,8 +215,8 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
       ss = __fmaf_rn(x.y, x.y, ss);
       w[i] = Act<A>::pack(x.x, x.y);
     }
-    // kept for the epilogue; written out with norm_out after the cluster barrier (whose release would
-    // otherwise wait for the global stores)
+    // kept for the epilogue, which writes it out with norm_out after the cluster exchange (the stores
+    // would otherwise sit between the items and the exchange on the critical path)
     res_s[it] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 
@@ -202,29 +229,25 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   __syncthreads();
   if (C > 1) cluster_wait_acquire();  // all CTAs of the cluster have started (arrived on entry)
   // Warp 0 reads the warp sums in parallel (lane i the i-th) and adds them in order with shuffles; with a
-  // cluster, lane c then writes the CTA's sum into slot `crank` of CTA c (C <= 16), so after one
-  // cluster barrier every CTA holds all the sums locally and adds them in rank order.
+  // cluster, lane c then sends the CTA's sum into slot `crank` of CTA c (C <= 16), so every CTA ends up
+  // holding all the sums locally and adds them in rank order.
   if (warp == 0) {
     const int nw = nthreads >> 5;
     const float mine = lane < nw ? red[lane] : 0.0f;
     float cta = 0.0f;
     for (int w = 0; w < nw; ++w) cta = __fadd_rn(cta, __shfl_sync(0xffffffffu, mine, w));
     if (C > 1) {
-      if (lane < static_cast<int>(C)) dsmem_store_f32(&red[34 + crank], static_cast<uint32_t>(lane), cta);
+      // Lane c sends the CTA's sum to slot `crank` of CTA c, counted on CTA c's exchange barrier; then
+      // warp 0 waits until its own barrier has all C sums and adds them in rank order.  A CTA leaves only
+      // after every peer's write into it has landed, and nothing is written into it after that.
+      if (lane < static_cast<int>(C)) st_async_f32(&red[34 + crank], static_cast<uint32_t>(lane), cta, xbar);
+      cluster_exchange_wait(xbar);
+      const float part = lane < static_cast<int>(C) ? red[34 + lane] : 0.0f;
+      float tot = 0.0f;
+      for (uint32_t c = 0; c < C; ++c) tot = __fadd_rn(tot, __shfl_sync(0xffffffffu, part, static_cast<int>(c)));
+      if (lane == 0) red[33] = tot;
     } else if (lane == 0) {
       red[33] = cta;
-    }
-  }
-  if (C > 1) {
-    // Every remote write is made before this barrier and none after it, so a CTA may exit as soon as
-    // it has passed the barrier.
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    if (warp == 0) {
-      const float mine = lane < static_cast<int>(C) ? red[34 + lane] : 0.0f;
-      float tot = 0.0f;
-      for (uint32_t c = 0; c < C; ++c) tot = __fadd_rn(tot, __shfl_sync(0xffffffffu, mine, static_cast<int>(c)));
-      if (lane == 0) red[33] = tot;
     }
   }
   __syncthreads();
@@ -334,6 +357,13 @@ int cluster_kernel_max_active_clusters(int act_dtype, int kc, const LaunchGeom& 
   if (act_dtype == MFR_BF16)
     return kc == 8 ? max_active_clusters<__nv_bfloat16, 8>(g) : max_active_clusters<__nv_bfloat16, 16>(g);
   return kc == 8 ? max_active_clusters<__half, 8>(g) : max_active_clusters<__half, 16>(g);
+}
+
+cudaError_t read_and_reset_cluster_timeouts(unsigned int* count) {
+  cudaError_t e = cudaMemcpyFromSymbol(count, g_cluster_wait_timeouts, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_cluster_wait_timeouts, &zero, sizeof(unsigned int));
 }
 
 }  // namespace mfr

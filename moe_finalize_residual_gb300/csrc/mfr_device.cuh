@@ -164,9 +164,6 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
@@ -174,11 +171,15 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 // Write a float into the shared memory of CTA `rank` of this cluster, at the address that `local` has
-// in this CTA (visible to that CTA after a cluster barrier with release/acquire semantics).
-__device__ __forceinline__ void dsmem_store_f32(float* local, uint32_t rank, float v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+// in this CTA, and count its 4 bytes on that CTA's mbarrier (at the address `local_bar` has here): the
+// receiver may read the value once that barrier's phase completes.
+__device__ __forceinline__ void st_async_f32(const float* local, uint32_t rank, float v, uint32_t local_bar) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+               "r"(__float_as_uint(v)), "r"(rb)
+               : "memory");
 }
 
 // Deterministic butterfly sum over the 32 lanes of a warp.

@@ -47,5 +47,6 @@ int cluster_kernel_blocks_per_sm(int act_dtype, int kc, const LaunchGeom& g);
 cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
 int stream_kernel_blocks_per_sm(int act_dtype, int groups, const LaunchGeom& g);
 cudaError_t read_and_reset_timeouts(unsigned int* count);
+cudaError_t read_and_reset_cluster_timeouts(unsigned int* count);
 
 }  // namespace mfr
