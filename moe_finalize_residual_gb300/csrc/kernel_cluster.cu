@@ -134,7 +134,6 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   }
   if (C > 1 && !p.fin_only) cluster_arrive_relaxed();
   int2* rt = reinterpret_cast<int2*>(smem + p.off_routes) + (in_group ? r : 0) * p.K;  // this partial's routes
-  if (p.pdl) pdl_launch_dependents();
   if (p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
   if (p.pdl) pdl_wait();
   if (!p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
@@ -181,6 +180,11 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   }
   cp_async_wait_all();
   __syncthreads();
+  // The next kernel on the stream may launch now (programmatic dependent launch).  Triggering here,
+  // after the gather, rather than at kernel start measured faster at 16 tokens (4.66 against 5.51 µs,
+  // L2-warm) and the same elsewhere: launched at start, the next launches' CTAs pile up on the SMs
+  // while this one still gathers.
+  if (p.pdl) pdl_launch_dependents();
 
   // The (chunk, vector) items of this CTA, spread over all its threads (item i to thread i mod the
   // block; consecutive threads take consecutive vectors): rank sum in order 0..R-1, residual add (kept
