@@ -392,11 +392,15 @@ def main():
             fn = finalize_fn(mfr, c, o)
             gg = capture_graph(lambda i: fn())
             us, _ = time_graph(gg, 50, 5)
+            fn_rr = finalize_fn(mfr, c, o, routing_ready=True)
+            gr = capture_graph(lambda i: fn_rr())
+            us_rr, _ = time_graph(gr, 50, 5)
             p = mfr.moe_finalize_plan([mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r])
                                        for r in range(c.R)], c.residual, c.gamma)
-            sweep.append({"T": T, "us": round(us, 3), "kernel": p["kernel"], "cluster": p["cluster"],
-                          "grid": p["grid"], "gbs_l2_warm": round(algorithmic_bytes(c) / (us * 1e-6) / 1e9, 1)})
-            del gg, c, o
+            sweep.append({"T": T, "us": round(us, 3), "us_routing_ready": round(us_rr, 3), "kernel": p["kernel"],
+                          "cluster": p["cluster"], "grid": p["grid"],
+                          "gbs_l2_warm": round(algorithmic_bytes(c) / (us * 1e-6) / 1e9, 1)})
+            del gg, gr, c, o
         gf = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=True))
         floor_pdl, _ = time_graph(gf, 50, 5)
         gf2 = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=False))
