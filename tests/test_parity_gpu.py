@@ -320,9 +320,9 @@ def test_overflow_and_cancellation(kernel, act):
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_pdl_on_off_bitwise_equal_over_many_routings(kernel):
     """flashinfer PR #6546, Description: outputs with PDL on are bitwise equal to PDL off over 900
-    routings (1-16 tokens, top-8).  Same here, also with the early routing read."""
+    routings (1-16 tokens, top-8).  The same count here, also with the early routing read."""
     n = 0
-    for seed in range(60):
+    for seed in range(150):
         for T in (1, 2, 5, 8, 13, 16):
             case = on_gpu(synth.make_case("pdl", T=T, H=2048, K=8, R=2, E=64, rsf=2.5, shared=True,
                                           seed_base=seed * 10_000))
@@ -332,7 +332,7 @@ def test_pdl_on_off_bitwise_equal_over_many_routings(kernel):
             assert np.array_equal(a.residual_out, b.residual_out) and np.array_equal(a.norm_out, b.norm_out)
             assert np.array_equal(a.residual_out, c.residual_out) and np.array_equal(a.norm_out, c.norm_out)
             n += 1
-    assert n == 360
+    assert n == 900
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
