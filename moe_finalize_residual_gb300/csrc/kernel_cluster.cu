@@ -3,8 +3,9 @@
 //
 // Design (prior art: flashinfer PR #6546, finalizeKernelSmallBatch, Description -- one CTA per
 // (token, hidden slice), 128-bit loads, top-K work split over thread groups combined through shared
-// memory, PDL trigger at kernel start; flashinfer PR #6631, Description -- load the indices and
-// scales of the routes first, then all rows, so the row loads are in flight together):
+// memory, PDL trigger at kernel start (here after the gather, which measured faster); flashinfer PR
+// #6631, Description -- load the indices and scales of the routes first, then all rows, so the row
+// loads are in flight together):
 //
 //  * a CTA covers NCH chunks of SV 16-byte vectors of the token's hidden row; its threads form R groups
 //    of SV, one group per partial: thread (r, v) owns vector v of each chunk of partial r.  With few
@@ -12,9 +13,11 @@
 //    CTAs per token loop over several chunks, so the grid stays about two CTAs per SM in one wave;
 //  * each thread reads the route indices and scales of its partial (the same addresses for the whole
 //    warp), then issues all its rows as 128-bit loads at once (up to KC in flight; K > KC repeats),
-//    plus its shared-expert row, and runs the FP32 fused multiply-add chain over them in route order:
-//    every partial row is produced by one thread in the definition's order, so it is bit-exact;
-//  * the shared-expert, residual and gamma slices of every chunk are copied into shared memory first;
+//    and runs the FP32 fused multiply-add chain over them in route order, then the factor and the
+//    shared-expert row: every partial row is produced by one thread in the definition's order, so it
+//    is bit-exact;
+//  * the shared-expert, residual and gamma slices of every chunk are copied into shared memory (by
+//    cp.async, before the row loads);
 //    each group writes its rounded partial rows to shared memory (one buffer per chunk, so one barrier
 //    serves all chunks); the (chunk, vector) items are then spread over all threads for the rank sum
 //    in order (the shared-memory combine) and the residual add, residual_out kept in shared memory;
