@@ -500,3 +500,49 @@ def test_finalize_out_with_fused_outputs(kernel):
     assert np.array_equal(bits16(fin), want["routed"])
     assert np.array_equal(bits16(ro), want["residual_out"])
     assert ulp_distance(bits16(no), want["norm_out"], case.act_dtype).max() <= 1
+
+
+# --------------------------------------------------------------------------------------------
+# Randomised shapes: many small problems drawn from a seeded generator, every kernel
+# --------------------------------------------------------------------------------------------
+
+def _random_shapes(n=36, seed=20261202):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        K = int(rng.choice([1, 2, 3, 6, 8, 10, 16, 22, 32, 64]))
+        R = int(rng.integers(1, 9))
+        if K * R > 128:
+            R = max(1, 128 // K)
+        H = int(rng.choice([8, 16, 40, 256, 1000, 2048, 3584, 6144, 7168])) // 8 * 8
+        if H % 16:
+            quant = "none"
+        else:
+            quant = str(rng.choice(["none", "fp8", "nvfp4"]))
+        out.append(dict(T=int(rng.integers(1, 70)), H=H, K=K, R=R, E=int(max(K, rng.integers(4, 80))),
+                        act=[torch.bfloat16, torch.float16][int(rng.integers(2))],
+                        sdt=[torch.float32, torch.bfloat16, torch.float16, None][int(rng.integers(4))],
+                        shared=bool(rng.integers(2)), mask=bool(rng.integers(2)), rsf=float(rng.choice([1.0, 2.5, 0.75])),
+                        quant=quant, layout=str(rng.choice(["row_major", "swizzled_128x4"])), seed=i))
+    return out
+
+
+@pytest.mark.parametrize("shape", _random_shapes(), ids=lambda s: f"T{s['T']}H{s['H']}K{s['K']}R{s['R']}{s['quant']}")
+def test_random_shapes_all_kernels(shape):
+    """Bit-exact residual_out, norm_out within 1 ulp and the oracle's quantiser on the kernel's own norm_out,
+    for every kernel, on small problems of random shape, dtype, masking and output mode."""
+    s = shape
+    case = synth.make_case("rnd", T=s["T"], H=s["H"], K=s["K"], R=s["R"], E=s["E"], act_dtype=s["act"],
+                           scale_dtype=s["sdt"], rsf=s["rsf"], shared=s["shared"], mask_quarter=s["mask"],
+                           seed_base=70_000 + 131 * s["seed"])
+    want = oracle.finalize(case)
+    qs = quant_scale_for(want["norm_out"], s["act"], s["quant"]) if s["quant"] != "none" else None
+    # A 1-ulp difference in one of a few hundred outputs moves the mean error by more than 1 %: small
+    # problems get a wider margin on that one statistic (every element is still held to 1 ulp).
+    slack = 0.01 if case.T * case.H >= 100_000 else 0.1
+    for kernel in KERNELS + ["auto"]:
+        res = run(on_gpu(case), kernel=kernel, quant=s["quant"], qscale=qs, sf_layout=s["layout"])
+        assert res.guards_ok, kernel
+        check_against_oracle(case, res, want, mae_slack=slack)
+        if s["quant"] != "none":
+            check_quant(res, s["act"], s["quant"], qs, s["layout"], case.T, case.H, want_norm=want["norm_out"])
