@@ -546,3 +546,14 @@ def test_random_shapes_all_kernels(shape):
         check_against_oracle(case, res, want, mae_slack=slack)
         if s["quant"] != "none":
             check_quant(res, s["act"], s["quant"], qs, s["layout"], case.T, case.H, want_norm=want["norm_out"])
+    # finalize-only mode on the same problem: the rounded rank sum, bit for bit
+    import moe_finalize_residual_gb300 as mfr
+    g = on_gpu(case)
+    for kernel in KERNELS + ["auto"]:
+        guard = Guarded(case.T * case.H * 2, "cuda", case.act_dtype, (case.T, case.H))
+        mfr.moe_finalize_routed(partials_of(g), routed_scaling_factor=case.rsf, out=guard.view, kernel=kernel)
+        torch.cuda.synchronize()
+        assert guard.guards_intact(), kernel
+        got = bits16(guard.view)
+        same = (got == want["routed"]) | (nan16(got, case.act_dtype) & nan16(want["routed"], case.act_dtype))
+        assert same.all(), f"{kernel}: finalize_out differs in {np.count_nonzero(~same)} elements"
