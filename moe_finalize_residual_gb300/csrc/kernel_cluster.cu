@@ -32,6 +32,8 @@
 #include "mfr_device.cuh"
 #include "mfr_launch.h"
 
+#include <atomic>
+
 namespace mfr {
 
 // The token's route table for partial P: entry k holds the row index of route k, or -1 for a route to
@@ -279,15 +281,15 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
 template <typename A, int KC>
 static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
   auto kern = cluster_finalize_kernel<A, KC>;
-  static int configured[64] = {0};
+  static std::atomic<int> configured[64] = {};  // per device: the attributes are set (once is enough)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+    if (dev < 64) configured[dev].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.grid, 1, 1);

@@ -34,6 +34,8 @@
 #include "mfr_device.cuh"
 #include "mfr_launch.h"
 
+#include <atomic>
+
 namespace mfr {
 
 __device__ unsigned int g_wait_timeouts = 0;
@@ -444,13 +446,13 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
 template <typename A, int G>
 static cudaError_t launch_stream(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
   auto kern = stream_finalize_kernel<A, G>;
-  static int configured[64] = {0};
+  static std::atomic<int> configured[64] = {};  // per device: the attributes are set (once is enough)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
     if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+    if (dev < 64) configured[dev].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.grid, 1, 1);
