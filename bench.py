@@ -511,7 +511,19 @@ def main():
                 if big:
                     row["frac"] = round(b / (us * 1e-6) / 1e9 / peak, 3)
                 rows_cfg.append(row)
-                del gg, o, c
+                del gg, o
+                if big:  # the quantised outputs of the bandwidth workload, at every size
+                    for quant, lay in (("fp8", "row_major"), ("nvfp4", "row_major"), ("nvfp4", "swizzled_128x4")):
+                        oq, qs = alloc_outs(mfr, c, quant, lay)
+                        fq = finalize_fn(mfr, c, oq, quant, qs, lay)
+                        gq = capture_graph(lambda i: fq(), n=4)
+                        uq, _ = time_graph(gq, 5, 2, launches=4)
+                        bq = algorithmic_bytes(c, quant)
+                        rows_cfg.append({**row, "out": quant if quant == "fp8" else f"nvfp4-{lay}", "us": round(uq, 3),
+                                         "gbs": round(bq / (uq * 1e-6) / 1e9, 1),
+                                         "frac": round(bq / (uq * 1e-6) / 1e9 / peak, 3)})
+                        del gq, oq
+                del c
             torch.cuda.empty_cache()
         extras["configs"] = rows_cfg
         extras["configs_wall_s"] = round(time.perf_counter() - t_cfg, 1)
