@@ -81,7 +81,7 @@ typedef enum {
 typedef enum {
   MFR_KERNEL_AUTO = 0,
   MFR_KERNEL_CLUSTER = 1, /* small batch: one thread-block cluster per token, hidden split over CTAs */
-  MFR_KERNEL_STREAM = 2   /* large batch: persistent CTAs, rows streamed by bulk copies             */
+  MFR_KERNEL_STREAM = 2   /* large batch: persistent CTAs, rows streamed by per-thread async copies */
 } mfr_kernel;
 
 /* Flags. */

@@ -1,5 +1,6 @@
 // Device-side pieces shared by the two finalize kernels: launch parameters, inline-PTX wrappers
-// (cp.async, bulk copies, mbarriers, cluster barriers and DSMEM, programmatic dependent launch),
+// (cp.async, mbarriers, cluster barriers, st.async into a peer's shared memory, programmatic dependent
+// launch),
 // activation-type traits, the residual step and the fused epilogue (RMSNorm output and FP8 / NVFP4
 // quantisation).
 //
