@@ -1,8 +1,7 @@
 // Device-side pieces shared by the two finalize kernels: launch parameters, inline-PTX wrappers
 // (cp.async, mbarriers, cluster barriers, st.async into a peer's shared memory, programmatic dependent
-// launch),
-// activation-type traits, the residual step and the fused epilogue (RMSNorm output and FP8 / NVFP4
-// quantisation).
+// launch), activation-type traits, the residual step and the fused epilogue (RMSNorm output and FP8 /
+// NVFP4 quantisation).
 //
 // Arithmetic follows the fused MoE finalize of flashinfer PR #6631 "perf(comm): gather MoE-finalize
 // routes together and accumulate in FP32" (Description) and TensorRT-LLM PR #16778 (Fix): FP32
