@@ -224,19 +224,29 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     const int smem = align_up(off_routes + R * a->K * 8, 16);
     if (smem > d.smem_optin) continue;
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
-    // clusters (of C CTAs; single CTAs when C = 1) the GPU holds at once
-    const auto key = std::make_tuple(dev, a->act_dtype * 2 + (kc == 8 ? 0 : 1), C, block, smem);
-    int n;
-    {
-      std::lock_guard<std::mutex> lock(g_mu);
-      auto it = g_cluster_ok.find(key);
-      n = (it == g_cluster_ok.end()) ? -1 : it->second;
-    }
-    if (n < 0) {
-      n = C > 1 ? cluster_kernel_max_active_clusters(a->act_dtype, kc, geo)
-                : d.sms * cluster_kernel_blocks_per_sm(a->act_dtype, kc, geo);
-      std::lock_guard<std::mutex> lock(g_mu);
-      g_cluster_ok[key] = n;
+    // clusters (of C CTAs; single CTAs when C = 1) the GPU holds at once, for a form
+    auto resident = [&](int f) {
+      const auto key = std::make_tuple(dev, a->act_dtype * 3 + f, C, block, smem);
+      int n;
+      {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_cluster_ok.find(key);
+        n = (it == g_cluster_ok.end()) ? -1 : it->second;
+      }
+      if (n < 0) {
+        n = C > 1 ? cluster_kernel_max_active_clusters(a->act_dtype, f, geo)
+                  : d.sms * cluster_kernel_blocks_per_sm(a->act_dtype, f, geo);
+        std::lock_guard<std::mutex> lock(g_mu);
+        g_cluster_ok[key] = n;
+      }
+      return n;
+    };
+    // One chunk: the wider register budget when it still runs in one wave, else the narrower one.
+    int form = kc == 16 ? kClusterForm16 : nch == 1 ? kClusterForm8OneChunk : kClusterForm8;
+    int n = resident(form);
+    if (form == kClusterForm8OneChunk && n < a->T) {
+      form = kClusterForm8;
+      n = resident(form);
     }
     if (n < 1) continue;
     const int64_t waves = (static_cast<int64_t>(a->T) + n - 1) / n;
@@ -246,6 +256,7 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     p->slice_vec = sv_fit;
     p->nchunk = nch;
     p->route_batch = kc;
+    p->cluster_form = form;
     p->off_red = off_red;
     p->off_routes = off_routes;
     *g = geo;

@@ -96,13 +96,14 @@ __device__ __forceinline__ void cluster_exchange_wait(uint32_t bar) {
 }
 
 // Resident CTAs the compiler must allow for (it sets the register budget): two 512-thread CTAs per SM
-// for the 8-routes-in-flight form.
+// for the 8-routes-in-flight form that loops over chunks; one for the other forms (the one-chunk form
+// runs small CTAs, which fit two to an SM all the same, and keeps more in registers).
 #ifndef MFR_CLUSTER_MIN_BLOCKS
 #define MFR_CLUSTER_MIN_BLOCKS 2
 #endif
 
-template <typename A, int KC>
-__global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_BLOCKS : 1) cluster_finalize_kernel(const __grid_constant__ KParams p) {
+template <typename A, int KC, int MINB>
+__global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
@@ -278,9 +279,9 @@ __global__ void __launch_bounds__(kClusterMaxThreads, KC <= 8 ? MFR_CLUSTER_MIN_
   }
 }
 
-template <typename A, int KC>
+template <typename A, int KC, int MINB>
 static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  auto kern = cluster_finalize_kernel<A, KC>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB>;
   static std::atomic<int> configured[64] = {};  // per device: the attributes are set (once is enough)
   int dev = 0;
   cudaGetDevice(&dev);
@@ -313,9 +314,9 @@ static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStr
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <typename A, int KC>
+template <typename A, int KC, int MINB>
 static int max_active_clusters(const LaunchGeom& g) {
-  auto kern = cluster_finalize_kernel<A, KC>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaLaunchConfig_t cfg = {};
@@ -337,9 +338,9 @@ static int max_active_clusters(const LaunchGeom& g) {
   return n;
 }
 
-template <typename A, int KC>
+template <typename A, int KC, int MINB>
 static int blocks_per_sm(const LaunchGeom& g) {
-  auto kern = cluster_finalize_kernel<A, KC>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, g.block, g.smem) != cudaSuccess) {
@@ -349,23 +350,45 @@ static int blocks_per_sm(const LaunchGeom& g) {
   return n;
 }
 
-// Routes in flight per thread (the plan's route_batch): 8, or 16 for larger top-k when that fits better.
+// The plan's form: routes in flight per thread and register budget (see ClusterForm).
+template <typename A>
+static cudaError_t launch_form(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
+  switch (p.cluster_form) {
+    case kClusterForm8: return launch_cluster<A, 8, MFR_CLUSTER_MIN_BLOCKS>(p, g, stream);
+    case kClusterForm8OneChunk: return launch_cluster<A, 8, 1>(p, g, stream);
+    default: return launch_cluster<A, 16, 1>(p, g, stream);
+  }
+}
+
 cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  if (act_dtype == MFR_BF16)
-    return p.route_batch == 8 ? launch_cluster<__nv_bfloat16, 8>(p, g, stream)
-                              : launch_cluster<__nv_bfloat16, 16>(p, g, stream);
-  return p.route_batch == 8 ? launch_cluster<__half, 8>(p, g, stream) : launch_cluster<__half, 16>(p, g, stream);
+  return act_dtype == MFR_BF16 ? launch_form<__nv_bfloat16>(p, g, stream) : launch_form<__half>(p, g, stream);
 }
 
-int cluster_kernel_blocks_per_sm(int act_dtype, int kc, const LaunchGeom& g) {
-  if (act_dtype == MFR_BF16) return kc == 8 ? blocks_per_sm<__nv_bfloat16, 8>(g) : blocks_per_sm<__nv_bfloat16, 16>(g);
-  return kc == 8 ? blocks_per_sm<__half, 8>(g) : blocks_per_sm<__half, 16>(g);
+template <typename A>
+static int blocks_per_sm_form(int form, const LaunchGeom& g) {
+  switch (form) {
+    case kClusterForm8: return blocks_per_sm<A, 8, MFR_CLUSTER_MIN_BLOCKS>(g);
+    case kClusterForm8OneChunk: return blocks_per_sm<A, 8, 1>(g);
+    default: return blocks_per_sm<A, 16, 1>(g);
+  }
 }
 
-int cluster_kernel_max_active_clusters(int act_dtype, int kc, const LaunchGeom& g) {
-  if (act_dtype == MFR_BF16)
-    return kc == 8 ? max_active_clusters<__nv_bfloat16, 8>(g) : max_active_clusters<__nv_bfloat16, 16>(g);
-  return kc == 8 ? max_active_clusters<__half, 8>(g) : max_active_clusters<__half, 16>(g);
+int cluster_kernel_blocks_per_sm(int act_dtype, int form, const LaunchGeom& g) {
+  return act_dtype == MFR_BF16 ? blocks_per_sm_form<__nv_bfloat16>(form, g) : blocks_per_sm_form<__half>(form, g);
+}
+
+template <typename A>
+static int max_active_clusters_form(int form, const LaunchGeom& g) {
+  switch (form) {
+    case kClusterForm8: return max_active_clusters<A, 8, MFR_CLUSTER_MIN_BLOCKS>(g);
+    case kClusterForm8OneChunk: return max_active_clusters<A, 8, 1>(g);
+    default: return max_active_clusters<A, 16, 1>(g);
+  }
+}
+
+int cluster_kernel_max_active_clusters(int act_dtype, int form, const LaunchGeom& g) {
+  return act_dtype == MFR_BF16 ? max_active_clusters_form<__nv_bfloat16>(form, g)
+                               : max_active_clusters_form<__half>(form, g);
 }
 
 cudaError_t read_and_reset_cluster_timeouts(unsigned int* count) {

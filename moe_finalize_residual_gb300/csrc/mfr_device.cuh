@@ -59,6 +59,7 @@ struct KParams {
   int32_t slice_vec;      // cluster kernel: 16-byte vectors per CTA per chunk (the last CTA may hold fewer)
   int32_t nchunk;         // cluster kernel: chunks of slice_vec vectors per CTA
   int32_t route_batch;    // cluster kernel: routes in flight per thread (8 or 16; larger top-k in rounds)
+  int32_t cluster_form;   // cluster kernel: the compiled form to launch (ClusterForm)
   int32_t off_routes;     // cluster kernel: shared-memory route table [R][K] (row index or -1, scale)
   int32_t off_red;
   // stream kernel

@@ -41,9 +41,12 @@ struct LaunchGeom {
 };
 
 cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
-// kc: routes in flight per thread, 8 (two 512-thread CTAs fit on an SM) or 16 (one)
-int cluster_kernel_max_active_clusters(int act_dtype, int kc, const LaunchGeom& g);
-int cluster_kernel_blocks_per_sm(int act_dtype, int kc, const LaunchGeom& g);
+// Cluster kernel forms: 8 routes in flight per thread with the register budget of two 512-thread CTAs
+// per SM (plans that loop over chunks); 8 in flight with a wider register budget (one-chunk plans, whose
+// CTAs are small); 16 in flight.
+enum ClusterForm { kClusterForm8 = 0, kClusterForm8OneChunk = 1, kClusterForm16 = 2 };
+int cluster_kernel_max_active_clusters(int act_dtype, int form, const LaunchGeom& g);
+int cluster_kernel_blocks_per_sm(int act_dtype, int form, const LaunchGeom& g);
 cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
 int stream_kernel_blocks_per_sm(int act_dtype, int groups, const LaunchGeom& g);
 cudaError_t read_and_reset_timeouts(unsigned int* count);
