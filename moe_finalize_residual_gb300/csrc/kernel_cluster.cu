@@ -21,11 +21,11 @@
 //    each group writes its rounded partial rows to shared memory (one buffer per chunk, so one barrier
 //    serves all chunks); the (chunk, vector) items are then spread over all threads for the rank sum
 //    in order (the shared-memory combine) and the residual add, residual_out kept in shared memory;
-//  * the sum of squares is reduced with warp shuffles, then across warps in shared memory, then across
-//    the cluster's CTAs: each CTA sends its sum into a slot of every peer's shared memory with st.async,
-//    counted on the peer's mbarrier, and once its own mbarrier has all C sums every CTA adds the slots
-//    in rank order, so all get the same deterministic total; then all threads write residual_out,
-//    norm_out and the quantised output.
+//  * the sum of squares is reduced with a warp butterfly, then a butterfly over the warp sums, then
+//    across the cluster's CTAs: each CTA sends its sum into a slot of every peer's shared memory with
+//    st.async, counted on the peer's mbarrier, and once its own mbarrier has all C sums every CTA adds
+//    the slots by the same fixed butterfly, so all get the same deterministic total; then all threads
+//    write residual_out, norm_out and the quantised output.
 //
 // No CTA waits on a flag in global memory.  Across CTAs there is the hardware cluster barrier at entry
 // (every CTA reaches it unconditionally) and the exchange's mbarrier, whose wait is bounded.
@@ -232,29 +232,24 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
 
   if (p.fin_only) return;  // finalize-only: no residual, RMSNorm or quantisation (the same for all threads)
 
-  // Sum of squares: warp shuffle, warps in order, then the cluster's CTAs in rank order.
+  // Sum of squares: a warp butterfly, then one over the warp sums, then one over the cluster's CTA
+  // sums.  Each butterfly has a fixed shape (lane i holds item i, zeros past the end), so the result is
+  // the same on every lane and every run, and every CTA of a cluster adds the same slots the same way.
   ss = warp_sum(ss);
   const int warp = tid >> 5, lane = tid & 31;
   if (lane == 0) red[warp] = ss;
   __syncthreads();
   if (C > 1) cluster_wait_acquire();  // all CTAs of the cluster have started (arrived on entry)
-  // Warp 0 reads the warp sums in parallel (lane i the i-th) and adds them in order with shuffles; with a
-  // cluster, lane c then sends the CTA's sum into slot `crank` of CTA c (C <= 16), so every CTA ends up
-  // holding all the sums locally and adds them in rank order.
   if (warp == 0) {
     const int nw = nthreads >> 5;
-    const float mine = lane < nw ? red[lane] : 0.0f;
-    float cta = 0.0f;
-    for (int w = 0; w < nw; ++w) cta = __fadd_rn(cta, __shfl_sync(0xffffffffu, mine, w));
+    const float cta = warp_sum(lane < nw ? red[lane] : 0.0f);
     if (C > 1) {
-      // Lane c sends the CTA's sum to slot `crank` of CTA c, counted on CTA c's exchange barrier; then
-      // warp 0 waits until its own barrier has all C sums and adds them in rank order.  A CTA leaves only
-      // after every peer's write into it has landed, and nothing is written into it after that.
+      // Lane c sends the CTA's sum to slot `crank` of CTA c (C <= 16), counted on CTA c's exchange
+      // barrier; then warp 0 waits until its own barrier has all C sums and adds them.  A CTA leaves
+      // only after every peer's write into it has landed, and nothing is written into it after that.
       if (lane < static_cast<int>(C)) st_async_f32(&red[34 + crank], static_cast<uint32_t>(lane), cta, xbar);
       cluster_exchange_wait(xbar);
-      const float part = lane < static_cast<int>(C) ? red[34 + lane] : 0.0f;
-      float tot = 0.0f;
-      for (uint32_t c = 0; c < C; ++c) tot = __fadd_rn(tot, __shfl_sync(0xffffffffu, part, static_cast<int>(c)));
+      const float tot = warp_sum(lane < static_cast<int>(C) ? red[34 + lane] : 0.0f);
       if (lane == 0) red[33] = tot;
     } else if (lane == 0) {
       red[33] = cta;
