@@ -181,6 +181,15 @@ def _build_args(partials: Sequence[Partial], residual, gamma, routed_scaling_fac
         for name, t in (("residual_out", residual_out), ("norm_out", norm_out), ("finalize_out", finalize_out)):
             if t is not None and (t.shape != (T, H) or t.dtype != act):
                 raise ValueError(f"{name} must be [{T}, {H}] {act}")
+        # The library gets plain pointers, so the quantised buffers' sizes are checked here.
+        qm = QUANT[quant_mode] if isinstance(quant_mode, str) else int(quant_mode)
+        if qm != 0:
+            need = {"quant_out": moe_finalize_quant_bytes(T, H, qm)}
+            if qm == QUANT["nvfp4"]:
+                need["sf_out"] = moe_finalize_sf_bytes(T, H, sf_layout)
+            for name, t in (("quant_out", quant_out), ("sf_out", sf_out)):
+                if name in need and t is not None and t.numel() * t.element_size() < need[name]:
+                    raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes; {need[name]} are written")
     else:
         for p in partials:
             if p.expert_scale is not None:

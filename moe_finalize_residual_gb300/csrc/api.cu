@@ -8,6 +8,7 @@
 // be NULL (same review: guard the prenormed output); 4 < topK <= 64 bounds the small-batch kernel
 // of flashinfer PR #6546 (here any 1 <= K <= 64 is accepted).
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -216,7 +217,7 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     const int sv = std::min(sv_soft, align_up(ceil_div(nvec, cg), unit));
     const int nch = ceil_div(nvec, cg * sv);
     const int C = ceil_div(nvec, nch * sv);
-    if (C > kMaxCluster) continue;
+    if (C > kMaxCluster || static_cast<int64_t>(a->T) * C > INT32_MAX) continue;  // grid.x is an int
     const int sv_fit = align_up(ceil_div(nvec, C * nch), unit);  // even slices
     const int block = align_up(sv_fit * R, 32);
     const int off_red = align_up((R + 2) * nch * sv_fit * 16, 16);

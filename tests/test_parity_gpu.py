@@ -424,6 +424,15 @@ def test_invalid_arguments_write_nothing():
         _call_without_sf(mfr, parts, case, out)
     with pytest.raises(ValueError):
         mfr.moe_finalize_fused(parts, case.residual.cpu(), case.gamma, residual_out=out.view)
+    # quantised buffers one byte short of what the call writes: refused before the launch
+    short_q = torch.empty(4 * 256 // 2 - 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError, match="quant_out"):
+        mfr.moe_finalize_fused(parts, case.residual, case.gamma, residual_out=out.view, quant_mode="nvfp4",
+                               quant_scale=1.0, quant_out=short_q)
+    short_sf = torch.empty(mfr.moe_finalize_sf_bytes(4, 256, "swizzled_128x4") - 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError, match="sf_out"):
+        mfr.moe_finalize_fused(parts, case.residual, case.gamma, residual_out=out.view, quant_mode="nvfp4",
+                               quant_scale=1.0, sf_layout="swizzled_128x4", sf_out=short_sf)
     torch.cuda.synchronize()
     assert out.guards_intact() and np.all(out.payload() == CANARY)
 
