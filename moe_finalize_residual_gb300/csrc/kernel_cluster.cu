@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
   uint4* xch = reinterpret_cast<uint4*>(smem);                // [NCH][R][SV] shared rows, then partial rows
   uint4* res_s = xch + NCH * p.R * SV;                        // [NCH][SV] residual slices, then residual_out
   uint4* gam_s = res_s + NCH * SV;                            // [NCH][SV] gamma slices
-  float* red = reinterpret_cast<float*>(smem + p.off_red);    // [0,32) warp sums, [32] CTA sum, [33] total,
+  float* red = reinterpret_cast<float*>(smem + p.off_red);    // [0,32) warp sums, [32,34) unused,
                                                               // [34,50) the cluster's CTA sums by rank,
                                                               // [52,54) the exchange's mbarrier
   const KPartial& P = p.part[in_group ? r : 0];
@@ -234,29 +234,30 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
 
   // Sum of squares: a warp butterfly, then one over the warp sums, then one over the cluster's CTA
   // sums.  Each butterfly has a fixed shape (lane i holds item i, zeros past the end), so the result is
-  // the same on every lane and every run, and every CTA of a cluster adds the same slots the same way.
+  // the same on every lane and every run, and every warp of every CTA of a cluster adds the same slots
+  // the same way: each warp computes the total itself, with no barrier after the exchange.
   ss = warp_sum(ss);
   const int warp = tid >> 5, lane = tid & 31;
+  const int nw = nthreads >> 5;
   if (lane == 0) red[warp] = ss;
   __syncthreads();
-  if (C > 1) cluster_wait_acquire();  // all CTAs of the cluster have started (arrived on entry)
-  if (warp == 0) {
-    const int nw = nthreads >> 5;
-    const float cta = warp_sum(lane < nw ? red[lane] : 0.0f);
-    if (C > 1) {
-      // Lane c sends the CTA's sum to slot `crank` of CTA c (C <= 16), counted on CTA c's exchange
-      // barrier; then warp 0 waits until its own barrier has all C sums and adds them.  A CTA leaves
-      // only after every peer's write into it has landed, and nothing is written into it after that.
+  float tot;
+  if (C > 1) {
+    cluster_wait_acquire();  // all CTAs of the cluster have started (arrived on entry)
+    // Lane c of warp 0 sends the CTA's sum to slot `crank` of CTA c (C <= 16), counted on CTA c's
+    // exchange barrier; every warp then waits until its own CTA's barrier has all C sums and adds them.
+    // A CTA leaves only after every peer's write into it has landed, and nothing is written into it
+    // after that.
+    if (warp == 0) {
+      const float cta = warp_sum(lane < nw ? red[lane] : 0.0f);
       if (lane < static_cast<int>(C)) st_async_f32(&red[34 + crank], static_cast<uint32_t>(lane), cta, xbar);
-      cluster_exchange_wait(xbar);
-      const float tot = warp_sum(lane < static_cast<int>(C) ? red[34 + lane] : 0.0f);
-      if (lane == 0) red[33] = tot;
-    } else if (lane == 0) {
-      red[33] = cta;
     }
+    cluster_exchange_wait(xbar);
+    tot = warp_sum(lane < static_cast<int>(C) ? red[34 + lane] : 0.0f);
+  } else {
+    tot = warp_sum(lane < nw ? red[lane] : 0.0f);
   }
-  __syncthreads();
-  const float rstd = rms_rstd(red[33], H, p.eps);
+  const float rstd = rms_rstd(tot, H, p.eps);
   {
     const float qscale = (p.quant != MFR_QUANT_NONE) ? *p.quant_scale : 1.0f;
     for (int base = 0; base < nitems; base += nthreads) {  // the same trip count for every thread (NVFP4 shuffles)
