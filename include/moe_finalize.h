@@ -92,7 +92,12 @@ enum {
   /* With MFR_FLAG_PDL: perm_idx and expert_scale were complete before the preceding kernel started,
    * so they may be read before the dependency wait (flashinfer PR #6546, PDL ordering item 1).  Do not
    * set it when the kernel right before this one writes the routing. */
-  MFR_FLAG_ROUTING_READY = 2u
+  MFR_FLAG_ROUTING_READY = 2u,
+  /* Test hook for failure detection: the cluster kernel's exchange barrier expects 4 bytes more than
+   * its peers send, so every wait on it runs out after its limit (about 2 s) and is counted by
+   * moe_finalize_read_timeouts.  The sums have all landed by then, so the outputs are still complete.
+   * It has no effect on plans with one CTA per token or on the stream kernel.  Not for production use. */
+  MFR_FLAG_TEST_EXCHANGE_TIMEOUT = 1u << 30
 };
 
 /* Status codes. */

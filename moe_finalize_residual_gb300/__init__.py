@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "Partial", "moe_finalize_fused", "moe_finalize_routed", "moe_finalize_plan", "moe_finalize_sf_bytes", "moe_finalize_quant_bytes",
     "moe_finalize_empty_launch", "moe_finalize_gather_floor_launch", "moe_finalize_read_timeouts", "moe_finalize_abi_version", "library_path",
-    "QUANT", "SF_LAYOUT", "KERNEL", "MFR_FLAG_PDL", "MFR_FLAG_ROUTING_READY",
+    "QUANT", "SF_LAYOUT", "KERNEL", "MFR_FLAG_PDL", "MFR_FLAG_ROUTING_READY", "MFR_FLAG_TEST_EXCHANGE_TIMEOUT",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -38,6 +38,7 @@ QUANT = {"none": 0, "fp8": 1, "nvfp4": 2}
 SF_LAYOUT = {"row_major": 0, "swizzled_128x4": 1}
 KERNEL = {"auto": 0, "cluster": 1, "stream": 2}
 MFR_FLAG_PDL, MFR_FLAG_ROUTING_READY = 1, 2
+MFR_FLAG_TEST_EXCHANGE_TIMEOUT = 1 << 30  # test hook: every cluster exchange wait runs out (see the C header)
 STATUS = {0: "MFR_OK", -1: "MFR_ERR_INVALID_ARG", -2: "MFR_ERR_UNSUPPORTED", -3: "MFR_ERR_CUDA"}
 
 
@@ -225,14 +226,15 @@ def moe_finalize_fused(partials: Sequence[Partial], residual: torch.Tensor, gamm
                        quant_out: Optional[torch.Tensor] = None, sf_out: Optional[torch.Tensor] = None,
                        pdl: bool = True, routing_ready: bool = False, kernel: str = "auto",
                        stream: Optional[torch.cuda.Stream] = None, check: bool = True,
-                       finalize_out: Optional[torch.Tensor] = None):
+                       finalize_out: Optional[torch.Tensor] = None, extra_flags: int = 0):
     """Enqueue the fused finalize on ``stream`` (default: the current stream).
 
     Outputs that are not passed in are allocated (``want_*`` = False leaves them out).  Returns
     ``(residual_out, norm_out, quant_out, sf_out)`` with None for outputs not produced.
     ``quant_scale`` is the FP8 encode scale or the NVFP4 global scale (a float or a 1-element tensor).
     ``finalize_out`` ([T, H] act), when given, also receives the finalized MoE output before the
-    residual (the rounded rank sum).
+    residual (the rounded rank sum).  ``extra_flags`` are further ``MFR_FLAG_*`` bits (the failure-detection
+    test hook ``MFR_FLAG_TEST_EXCHANGE_TIMEOUT``).
     """
     T, H = residual.shape
     dev = residual.device
@@ -253,7 +255,7 @@ def moe_finalize_fused(partials: Sequence[Partial], residual: torch.Tensor, gamm
             sf_out = torch.empty(int(moe_finalize_sf_bytes(T, H, sf_layout)), dtype=torch.uint8, device=dev)
     else:
         quant_scale = None
-    flags = (MFR_FLAG_PDL if pdl else 0) | (MFR_FLAG_ROUTING_READY if routing_ready else 0)
+    flags = (MFR_FLAG_PDL if pdl else 0) | (MFR_FLAG_ROUTING_READY if routing_ready else 0) | int(extra_flags)
     a, keep = _build_args(partials, residual, gamma, routed_scaling_factor, eps, residual_out, norm_out, qm,
                           quant_scale, sf_layout, quant_out, sf_out, flags, kernel, check=check,
                           finalize_out=finalize_out)

@@ -84,7 +84,7 @@ int validate(const mfr_args* a) {
       return fail(MFR_ERR_UNSUPPORTED, "sf_layout %d: only ROW_MAJOR and SWIZZLED_128x4", a->sf_layout);
     if (a->H % 16 != 0) return fail(MFR_ERR_INVALID_ARG, "NVFP4 needs H %% 16 == 0 (H = %d)", a->H);
   }
-  if (a->flags & ~static_cast<uint32_t>(MFR_FLAG_PDL | MFR_FLAG_ROUTING_READY))
+  if (a->flags & ~static_cast<uint32_t>(MFR_FLAG_PDL | MFR_FLAG_ROUTING_READY | MFR_FLAG_TEST_EXCHANGE_TIMEOUT))
     return fail(MFR_ERR_INVALID_ARG, "unknown flag bits 0x%x", a->flags);
   if (a->kernel < MFR_KERNEL_AUTO || a->kernel > MFR_KERNEL_STREAM)
     return fail(MFR_ERR_INVALID_ARG, "kernel %d unknown", a->kernel);
@@ -259,6 +259,8 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     p->route_batch = kc;
     p->cluster_form = form;
     p->off_red = off_red;
+    // 4 bytes from every CTA of the cluster (and 4 that never come under the timeout test hook)
+    p->xch_tx_bytes = 4u * C + ((a->flags & MFR_FLAG_TEST_EXCHANGE_TIMEOUT) ? 4u : 0u);
     p->off_routes = off_routes;
     *g = geo;
     *waves_out = waves;

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
   if (C > 1 && !p.fin_only && tid == 0) {
     mbar_init(xbar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(xbar, 4u * C);
+    mbar_arrive_expect_tx(xbar, p.xch_tx_bytes);
   }
   if (C > 1 && !p.fin_only) cluster_arrive_relaxed();
   int2* rt = reinterpret_cast<int2*>(smem + p.off_routes) + (in_group ? r : 0) * p.K;  // this partial's routes

@@ -62,6 +62,7 @@ struct KParams {
   int32_t cluster_form;   // cluster kernel: the compiled form to launch (ClusterForm)
   int32_t off_routes;     // cluster kernel: shared-memory route table [R][K] (row index or -1, scale)
   int32_t off_red;
+  uint32_t xch_tx_bytes;  // cluster kernel: bytes the exchange barrier expects (4 per CTA of the cluster)
   // stream kernel
   int32_t chunk;          // hidden elements per pass
   int32_t stages;         // row buffers in the ring

@@ -71,7 +71,7 @@ class Result:
 
 
 def run(case, kernel="auto", pdl=True, routing_ready=False, quant="none", qscale=None, sf_layout="row_major",
-        residual_out=True, norm_out=True, stream=None) -> Result:
+        residual_out=True, norm_out=True, stream=None, extra_flags=0) -> Result:
     """Run the library on a device-resident case with canary-guarded outputs."""
     import moe_finalize_residual_gb300 as mfr
     dev = case.device
@@ -89,7 +89,8 @@ def run(case, kernel="auto", pdl=True, routing_ready=False, quant="none", qscale
                            norm_out=None if no is None else no.view, want_residual_out=False, want_norm_out=False,
                            quant_mode=quant, quant_scale=qscale, sf_layout=sf_layout,
                            quant_out=None if qo is None else qo.view, sf_out=None if sf is None else sf.view,
-                           pdl=pdl, routing_ready=routing_ready, kernel=kernel, stream=stream)
+                           pdl=pdl, routing_ready=routing_ready, kernel=kernel, stream=stream,
+                           extra_flags=extra_flags)
     torch.cuda.synchronize()
     ok = all(g.guards_intact() for g in (ro, no, qo, sf) if g is not None)
     return Result(bits16(ro.view) if ro else None, bits16(no.view) if no else None,

@@ -450,6 +450,27 @@ def test_no_wait_timed_out():
     assert mfr.moe_finalize_read_timeouts() == 0
 
 
+def test_exchange_wait_that_runs_out_is_counted():
+    """Failure detection on the GPU without a fault: the test hook makes the cluster exchange barrier
+    expect 4 bytes that no peer sends (a signal that never comes), so every warp's wait on it runs out
+    after its limit (about 2 s), is counted, and the kernel returns.  The context stays usable: the sums
+    had all landed, so the outputs still match the oracle, and a normal call afterwards counts nothing."""
+    import moe_finalize_residual_gb300 as mfr
+    assert mfr.moe_finalize_read_timeouts() == 0
+    case = synth.make_case("timeout", T=2, H=6144, K=8, R=4, E=64, rsf=2.5, shared=True)
+    g = on_gpu(case)
+    plan = mfr.moe_finalize_plan(partials_of(g), g.residual, g.gamma, kernel="cluster")
+    assert plan["kernel"] == "cluster" and plan["cluster"] > 1, plan
+    t0 = time.monotonic()
+    res = run(g, kernel="cluster", extra_flags=mfr.MFR_FLAG_TEST_EXCHANGE_TIMEOUT)
+    elapsed = time.monotonic() - t0
+    assert mfr.moe_finalize_read_timeouts() == plan["grid"] * (plan["block"] // 32)  # every warp of every CTA
+    assert 1.0 < elapsed < 60.0, elapsed
+    check_against_oracle(case, res)
+    check_against_oracle(case, run(g, kernel="cluster"))
+    assert mfr.moe_finalize_read_timeouts() == 0
+
+
 # ------------------------------------------------------------------------------------------------------
 # Finalize-only mode: the rounded rank sum S (p_0 for one partial), no residual / RMSNorm / quant.
 
