@@ -456,6 +456,37 @@ def test_fp8_quant_simple():
     assert q[0][4] == 0x7E and q[0][5] == 0x80
 
 
+def test_fp8_scaled_hand_worked():
+    """The FP8 output applies the per-tensor scale as an encode scale, q = e4m3(v * s): blocks worked by
+    hand from the OCP E4M3 definition with s = 0.75 and s = 448/3 (ties, subnormal ties, saturation after
+    scaling, signed zero)."""
+    g = json.load(open(os.path.join(GOLDEN, "fp8_scaled.json")))
+    for case in g["cases"]:
+        v = torch.tensor([case["values"]], dtype=torch.float32).to(torch.bfloat16)
+        assert torch.equal(v.float(), torch.tensor([case["values"]])), "fixture values must be exact in bf16"
+        q, _ = oracle.quantize(v.view(torch.int16).numpy().view(np.uint16), torch.bfloat16, oracle.QUANT_FP8,
+                               case["scale"])
+        assert list(q[0]) == case["bytes"], (case["scale"], list(q[0]))
+
+
+@pytest.mark.parametrize("act", [torch.bfloat16, torch.float16])
+def test_fp8_scaled_matches_torch(act):
+    """e4m3 of the fp32 product v * s by torch's own conversion (products kept below 464, where torch's
+    float8_e4m3fn conversion rounds like the saturating encoder), for a small scale and for 448 / amax."""
+    gen = torch.Generator().manual_seed(21)
+    x = (torch.randn(8, 512, generator=gen) * 2.5).to(act)
+    amax = float(x.float().abs().max())
+    for s in (0.37, 448.0 / amax, 3.0):
+        s32 = float(np.float32(s))
+        prod = x.float() * s32
+        keep = prod.abs() < 464
+        q, _ = oracle.quantize(x.view(torch.int16).numpy().view(np.uint16), act, oracle.QUANT_FP8, s32)
+        want = prod.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert keep.float().mean() > 0.5
+        assert np.array_equal(q[keep.numpy()], want[keep.numpy()]), s
+        assert np.all(q[~keep.numpy()] & 0x7F == 0x7E)  # the rest saturates to +-448
+
+
 def test_sf_layouts():
     g = json.load(open(os.path.join(GOLDEN, "nvfp4_block.json")))["swizzled_128x4_offsets"]
     for m, k, off in g["pairs"]:
@@ -496,6 +527,8 @@ MUTANTS = {
     "masked route read": ("if (idx < 0 || (int64_t)idx >= P->rows) continue;            /* masked route */",
                           "if (idx < 0) idx = 0;"),
     "nibbles swapped": ("q[j] = (uint8_t)(lo | (hi << 4));", "q[j] = (uint8_t)(hi | (lo << 4));"),
+    "fp8 scale ignored": ("float p = v * qscale;", "float p = v;"),
+    "fp8 scale divides": ("float p = v * qscale;", "float p = v / qscale;"),
     "sf from unscaled amax": ("float sf_in = (amax / 6.0f) * qscale;", "float sf_in = amax * qscale;"),
     "swizzle rows swapped": ("return tile * 512 + (r % 32) * 16 + (r / 32) * 4 + (k % 4);",
                              "return tile * 512 + (r / 4) * 16 + (r % 4) * 4 + (k % 4);"),
@@ -513,6 +546,7 @@ def all_pins():
         ("constant row", lambda: [test_rmsnorm_constant_row(c) for c in (0.003, 0.5)]),
         ("unit rms", test_rmsnorm_unit_rms_before_gamma),
         ("nvfp4 block", test_nvfp4_hand_worked_block),
+        ("fp8 scaled", test_fp8_scaled_hand_worked),
         ("sf layout", test_sf_layouts),
     ]
     for name, fn in checks:
