@@ -1,16 +1,18 @@
 """Benchmark of the fused MoE finalize + rank sum + residual + RMSNorm on GB300.
 
-Headline (one JSON line on stdout): microseconds per call of the decode workload -- hidden 6144,
-256 experts, top-8, four tensor-parallel partials resident in this GPU's memory, each with its own
-GEMM2 rows, softmax top-k weights and shared-expert output; routed_scaling_factor 2.5, bf16 -- at
-128 tokens.  As in the benchmark of flashinfer PR #6631 (fi_finalize_bench.py), one step is one
-replay of a CUDA graph of 20 back-to-back launches (launched with PDL); each launch reads a
-different one of several input sets whose total size is over three times the L2, so every launch
-streams its inputs from HBM.  Also reported: the whole token sweep 1..128 (L2-warm, the page's own
-setting), the launch floor, the bandwidth workload (hidden 7168, 16384 tokens), the end-to-end time
-through the public API with host buffers, and the CPU oracle on the host cores.
+Headline (the last stdout line, one compact JSON object): microseconds per call of the decode
+workload -- hidden 6144, 256 experts, top-8, four tensor-parallel partials resident in this GPU's
+memory, each with its own GEMM2 rows, softmax top-k weights and shared-expert output;
+routed_scaling_factor 2.5, bf16 -- at 128 tokens.  As in the benchmark of flashinfer PR #6631
+(fi_finalize_bench.py), one step is one replay of a CUDA graph of 20 back-to-back launches (launched
+with PDL); each launch reads a different one of several input sets whose total size is over three
+times the L2, so every launch streams its inputs from HBM.  The line carries the roofline, the
+end-to-end time through the public API with host buffers, the CPU oracle on the host cores and a few
+summary scalars.  The extras -- the token sweep 1..128 (L2-warm, the page's own setting) against the
+launch floor, every case of the tiny, masked, high-top-k and bandwidth workloads, the finalize-only
+mode and the unfused pair -- are written as JSON to the file named by --extras-out.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--extras-out PATH]
 """
 from __future__ import annotations
 
@@ -153,9 +155,12 @@ def time_graph(g, reps, warmup, launches=GRAPH_LAUNCHES):
     return statistics.median(times), times
 
 
-def make_sets(T, nsets, device, base=HEADLINE):
-    return [synth.make_case(f"decode-T{T}-set{i}", T=T, device=device, **{**base, "seed_base": base["seed_base"]
-                                                                           + 7919 * i}) for i in range(nsets)]
+def make_sets(T, nsets, device, base=HEADLINE, tok0=0):
+    """`nsets` independent draws of the T-token workload; `tok0` (the first token of this rank's range
+    of a multi-rank batch) offsets the seeds so every rank draws different tokens."""
+    return [synth.make_case(f"decode-T{T}-set{i}", T=T, device=device,
+                            **{**base, "seed_base": base["seed_base"] + 7919 * i + 104_729 * tok0})
+            for i in range(nsets)]
 
 
 def finalize_fn(mfr, case, outs, quant="none", qscale=None, sf_layout="row_major", kernel="auto",
@@ -234,9 +239,8 @@ def cpu_baseline(case, budget_s=8.0):
     all_us, n2, el2 = timed(lambda: oracle.finalize_threads(c, threads))
     return {"value": all_us, "unit": UNIT, "cores": threads, "kind": "oracle",
             "single_core_value": one_us,
-            "sample": f"whole calls of the headline workload (T={c.T}, H={c.H}, R={c.R}, K={c.K}): {n2} calls in "
-                      f"{el2:.1f} s with the tokens split over {threads} host threads; single_core_value: {n1} "
-                      f"calls in {el1:.1f} s on one core"}
+            "sample": f"whole T={c.T} calls: {n2} in {el2:.1f} s, tokens over {threads} threads; one core: "
+                      f"{n1} in {el1:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -298,13 +302,277 @@ def run_case(spec: str, reps: int):
                       "plan": p}), flush=True)
 
 
+def headline_region(g, steps, world, dev, local):
+    """The K timed steps between barriers, clocks sampled meanwhile: (total ms, median µs per launch,
+    wall s, clock summary), the times the maximum over ranks."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for a, b in evs:
+            a.record()
+            g.replay()
+            b.record()
+        stop.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    med = statistics.median([a.elapsed_time(b) * 1000.0 / GRAPH_LAUNCHES for a, b in evs])
+    if world > 1:
+        t = torch.tensor([total_ms, med], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, med = float(t[0]), float(t[1])
+    return total_ms, med, wall, clk.summary()
+
+
+def throttled(c):
+    """A throttle reason that invalidates a timing, or SM clocks well below their maximum with none."""
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"} & set(c["reasons"])
+    low = c["sm_mhz"] is not None and c["sm_max_mhz"] and c["sm_mhz"] < 0.85 * c["sm_max_mhz"] and not c["reasons"]
+    return bool(bad) or bool(low)
+
+
+def extra_sweep(mfr, dev, peak, sets, outs, nsets, bytes_call):
+    """The headline again with the early routing read, the L2-warm token sweep 1..128 (the pages'
+    setting) and the two launch floors."""
+    ex = {}
+    # Safe here and in a MoE layer: the routing is written long before the GEMM that precedes the
+    # finalize, and back-to-back finalize launches do not write it.  Same rotating input sets.
+    calls_rr = [finalize_fn(mfr, c, o, routing_ready=True) for c, o in zip(sets, outs)]
+    grr = capture_graph(lambda i: calls_rr[i % nsets]())
+    rr_us, _ = time_graph(grr, 200, 20)
+    ex["headline_routing_ready"] = {"us": round(rr_us, 3), "gbs": round(bytes_call / (rr_us * 1e-6) / 1e9, 1),
+                                    "frac": round(bytes_call / (rr_us * 1e-6) / 1e9 / peak, 4)}
+    del grr, calls_rr
+    sweep = []
+    for T in (1, 4, 16, 32, 64, 128):
+        c = make_sets(T, 1, dev)[0]
+        o = alloc_outs(mfr, c)[0]
+        fn = finalize_fn(mfr, c, o)
+        gg = capture_graph(lambda i: fn())
+        us, _ = time_graph(gg, 50, 5)
+        fn_rr = finalize_fn(mfr, c, o, routing_ready=True)
+        gr = capture_graph(lambda i: fn_rr())
+        us_rr, _ = time_graph(gr, 50, 5)
+        p = mfr.moe_finalize_plan([mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r])
+                                   for r in range(c.R)], c.residual, c.gamma)
+        b = algorithmic_bytes(c)
+        sweep.append({"T": T, "us": round(us, 3), "us_routing_ready": round(us_rr, 3), "kernel": p["kernel"],
+                      "cluster": p["cluster"], "grid": p["grid"], "bytes": b,
+                      "gbs_l2_warm": round(b / (us * 1e-6) / 1e9, 1)})
+        del gg, gr, c, o
+    gf = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=True))
+    floor_pdl, _ = time_graph(gf, 50, 5)
+    gf2 = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=False))
+    floor_nopdl, _ = time_graph(gf2, 50, 5)
+    # the dependent index -> row -> store chain alone (20 rows, one per launch: L2-warm like the sweep)
+    rows = torch.zeros(1024, 6144, dtype=torch.bfloat16, device=dev)
+    gidx = torch.randint(0, rows.shape[0], (GRAPH_LAUNCHES, 1), dtype=torch.int32, device=dev)
+    gout = torch.empty(512, dtype=torch.uint8, device=dev)
+    gf3 = capture_graph(lambda i: mfr.moe_finalize_gather_floor_launch(gidx[i], rows, gout, pdl=True))
+    floor_gather, _ = time_graph(gf3, 50, 5)
+    del gf, gf2, gf3, rows
+    for s in sweep:
+        # the launch-bound floor: an empty PDL launch plus the call's bytes at the peak bandwidth
+        fl = floor_pdl + s["bytes"] / (peak * 1e9) * 1e6
+        s["floor_us"] = round(fl, 3)
+        s["x_floor"] = round(s["us"] / fl, 2)
+        s["x_gather_floor"] = round(s["us"] / floor_gather, 2)
+    ex["sweep_l2_warm"] = sweep
+    ex["launch_floor_us"] = {"pdl": round(floor_pdl, 3), "no_pdl": round(floor_nopdl, 3),
+                             "gather_chain_pdl": round(floor_gather, 3)}
+    return ex
+
+
+def extra_unfused(mfr, dev):
+    """Finalize-only, and fused vs unfused (finalize, then residual + RMSNorm), L2-warm graphs of 20
+    launches (the pages' setting).  The unfused pair's second launch is this library's fused call on
+    one partial whose route is masked and whose shared row is the first launch's output S, with factor
+    1: it reads S, the residual and gamma and writes residual_out and norm_out, the work of a separate
+    residual-RMSNorm kernel; its outputs are compared with the fused call's."""
+    fin = []
+    for (H, E, K, R, shared, T) in ((6144, 256, 8, 4, True, 1), (6144, 256, 8, 4, True, 16),
+                                    (6144, 256, 8, 4, True, 128), (2048, 512, 22, 1, False, 16),
+                                    (3584, 896, 16, 1, False, 16), (4096, 512, 32, 1, False, 16),
+                                    (4096, 512, 32, 1, False, 128)):
+        c = synth.make_case("fin", T=T, H=H, E=E, K=K, R=R, rsf=2.5, shared=shared, device=dev,
+                            scale_dtype=torch.float32 if R == 1 else torch.bfloat16, seed_base=500_000)
+        parts = [mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r]) for r in range(c.R)]
+        o = alloc_outs(mfr, c)[0]
+        s_out = torch.empty_like(c.residual)
+        masked = torch.full((T, 1), -1, dtype=torch.int32, device=dev)
+        second = [mfr.Partial(c.gemm2[0][:1], masked, None, s_out)]
+        ro2, no2 = torch.empty_like(c.residual), torch.empty_like(c.residual)
+
+        def fused(i):
+            mfr.moe_finalize_fused(parts, c.residual, c.gamma, routed_scaling_factor=c.rsf, eps=c.eps,
+                                   residual_out=o[0], norm_out=o[1], check=False)
+
+        def fin_only(i):
+            mfr.moe_finalize_routed(parts, routed_scaling_factor=c.rsf, out=s_out, check=False)
+
+        def unfused(i):
+            fin_only(i)
+            mfr.moe_finalize_fused(second, c.residual, c.gamma, routed_scaling_factor=1.0, eps=c.eps,
+                                   residual_out=ro2, norm_out=no2, check=False)
+        res = {}
+        for name, fn in (("fused_us", fused), ("finalize_only_us", fin_only), ("unfused_pair_us", unfused)):
+            gg = capture_graph(fn)
+            res[name], _ = time_graph(gg, 50, 5)
+            del gg
+        torch.cuda.synchronize()
+
+        def ordinal(x):  # 16-bit float bit patterns as an ordered integer line (+0 and -0 equal)
+            b = x.view(torch.int16).to(torch.int32)
+            return torch.where(b < 0, -(b & 0x7FFF), b)
+        same = bool(torch.equal(o[0], ro2))
+        norm_ulp = int((ordinal(o[1]) - ordinal(no2)).abs().max())
+        fb = algorithmic_bytes(c, finalize_only=True)
+        fin.append({"H": H, "K": K, "R": R, "T": T, **{k: round(v, 3) for k, v in res.items()},
+                    "finalize_only_gbs_l2_warm": round(fb / (res["finalize_only_us"] * 1e-6) / 1e9, 1),
+                    "unfused_over_fused": round(res["unfused_pair_us"] / res["fused_us"], 3),
+                    "unfused_residual_out_equal": same, "unfused_norm_out_max_ulp": norm_ulp})
+        del c, parts, o, s_out, second, ro2, no2
+    torch.cuda.empty_cache()
+    return {"finalize_only_and_unfused_l2_warm": fin}
+
+
+def extra_configs(mfr, dev, peak):
+    """Every case of the tiny, masked and high-top-k workloads (L2-warm, like the pages' latency
+    tables) and the bandwidth workload's H x T grid (inputs larger than L2) with every output form."""
+    t_cfg = time.perf_counter()
+    rows_cfg = []
+    for fam in ("tiny", "masked", "highk", "bandwidth"):
+        for c in synth.config_cases(fam, device=dev):
+            o = alloc_outs(mfr, c)[0]
+            fn = finalize_fn(mfr, c, o)
+            big = fam == "bandwidth"
+            gg = capture_graph(lambda i: fn(), n=4 if big else GRAPH_LAUNCHES)
+            us, _ = time_graph(gg, 5 if big else 30, 2 if big else 3, launches=4 if big else GRAPH_LAUNCHES)
+            p = mfr.moe_finalize_plan([mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r])
+                                       for r in range(c.R)], c.residual, c.gamma)
+            b = algorithmic_bytes(c)
+            row = {"family": fam, "T": c.T, "H": c.H, "K": c.K, "R": c.R,
+                   "act": str(c.act_dtype).replace("torch.", ""),
+                   "scale": str(c.scale_dtype).replace("torch.", ""), "kernel": p["kernel"], "us": round(us, 3),
+                   "gbs": round(b / (us * 1e-6) / 1e9, 1), "l2": "inputs > L2" if big else "warm"}
+            if big:
+                row["out"] = "bf16"
+                row["frac"] = round(b / (us * 1e-6) / 1e9 / peak, 3)
+            rows_cfg.append(row)
+            del gg, o
+            if big:  # the quantised outputs of the bandwidth workload, at every size
+                for quant, lay in (("fp8", "row_major"), ("nvfp4", "row_major"), ("nvfp4", "swizzled_128x4")):
+                    oq, qs = alloc_outs(mfr, c, quant, lay)
+                    fq = finalize_fn(mfr, c, oq, quant, qs, lay)
+                    gq = capture_graph(lambda i: fq(), n=4)
+                    uq, _ = time_graph(gq, 5, 2, launches=4)
+                    bq = algorithmic_bytes(c, quant)
+                    rows_cfg.append({**row, "out": quant if quant == "fp8" else f"nvfp4-{lay}", "us": round(uq, 3),
+                                     "gbs": round(bq / (uq * 1e-6) / 1e9, 1),
+                                     "frac": round(bq / (uq * 1e-6) / 1e9 / peak, 3)})
+                    del gq, oq
+            del c
+        torch.cuda.empty_cache()
+    return {"configs": rows_cfg, "configs_wall_s": round(time.perf_counter() - t_cfg, 1)}
+
+
+def e2e_headline(mfr, dev, tok0):
+    """End to end through the public API with host buffers.  Every input of a step sits in one pinned
+    host buffer and the device tensors are views of one device buffer (256-byte aligned slices), so a
+    step is one host-to-device copy, the fused call and one device-to-host copy of residual_out and
+    norm_out."""
+    c = make_sets(HEADLINE_T, 1, dev, tok0=tok0)[0]
+    inputs = [*c.gemm2, *c.perm, *c.scale, *c.shared, c.residual, c.gamma]
+    sizes = [-(-t.numel() * t.element_size() // 256) * 256 for t in inputs]
+    host_in = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
+    views, off = [], 0
+    for t, n in zip(inputs, sizes):
+        nb = t.numel() * t.element_size()
+        host_in[off:off + nb].view(t.dtype).view(t.shape).copy_(t.cpu())
+        views.append(dev_in[off:off + nb].view(t.dtype).view(t.shape))
+        off += n
+    R = c.R
+    g2, pm, sc, sh = views[:R], views[R:2 * R], views[2 * R:3 * R], views[3 * R:4 * R]
+    res_v, gam_v = views[4 * R], views[4 * R + 1]
+    parts_e2e = [mfr.Partial(g2[r], pm[r], sc[r], sh[r]) for r in range(R)]
+    out_bytes = c.residual.numel() * 2
+    dev_out = torch.empty(2 * out_bytes, dtype=torch.uint8, device=dev)
+    host_out = torch.empty(2 * out_bytes, dtype=torch.uint8).pin_memory()
+    ro_v = dev_out[:out_bytes].view(c.residual.dtype).view(c.residual.shape)
+    no_v = dev_out[out_bytes:].view(c.residual.dtype).view(c.residual.shape)
+    h2d = sum(t.numel() * t.element_size() for t in inputs)
+    d2h = 2 * out_bytes
+
+    # (splitting the input copy over 2-8 streams measured no faster: the host link is the limit)
+    def e2e_step():
+        dev_in.copy_(host_in, non_blocking=True)
+        mfr.moe_finalize_fused(parts_e2e, res_v, gam_v, routed_scaling_factor=c.rsf, eps=c.eps,
+                               residual_out=ro_v, norm_out=no_v)
+        host_out.copy_(dev_out, non_blocking=True)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = 50
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n_e2e):
+        e2e_step()
+    b.record()
+    torch.cuda.synchronize()
+    e2e_us = a.elapsed_time(b) * 1000.0 / n_e2e
+    # the host copy of the result equals the same call on the original device tensors
+    ref_ro, ref_no, _, _ = mfr.moe_finalize_fused(
+        [mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r]) for r in range(R)], c.residual, c.gamma,
+        routed_scaling_factor=c.rsf, eps=c.eps)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(host_out[:out_bytes], ref_ro.view(torch.uint8).reshape(-1).cpu()) and
+                torch.equal(host_out[out_bytes:], ref_no.view(torch.uint8).reshape(-1).cpu()))
+    e2e = {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "copies_per_step": 2, "h2d_gbs": round(h2d / (e2e_us * 1e-6) / 1e9, 1),
+           "result_equals_device_resident_call": same}
+    return e2e, c
+
+
+def summary_of(extras):
+    """A few scalars from the extras for the headline line (the full lists go to --extras-out): L2-warm
+    µs and the multiple of the launch-bound floor at 1 and 16 tokens, and fractions of the HBM peak on
+    the bandwidth workload (hidden, tokens, output)."""
+    s = {}
+    sw = {r["T"]: r for r in extras.get("sweep_l2_warm", [])}
+    for T in (1, 16):
+        if T in sw:
+            s[f"T{T}_us"] = sw[T]["us"]
+            s[f"T{T}_x_floor"] = sw[T]["x_floor"]
+    want = {(6144, 1024, "bf16"), (7168, 1024, "bf16"), (7168, 16384, "bf16"), (7168, 16384, "nvfp4-swizzled_128x4")}
+    for r in extras.get("configs", []):
+        if r["family"] == "bandwidth" and (r["H"], r["T"], r["out"]) in want:
+            s[f"frac_H{r['H']}_T{r['T']}_{r['out'].split('-')[0]}"] = r["frac"]
+    for r in extras.get("finalize_only_and_unfused_l2_warm", []):
+        if r["H"] == 6144 and r["T"] == 128:
+            s["unfused_over_fused_T128"] = r["unfused_over_fused"]
+    return s
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-extras", action="store_true", help="headline only (no sweep, bandwidth, e2e, cpu)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the sweep, config and bandwidth extras (the headline, e2e and cpu_baseline stay)")
+    ap.add_argument("--extras-out", default=None, metavar="PATH",
+                    help="write the extras (sweep, every config case, bandwidth grid, unfused pair) as JSON here")
+    ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle time per cpu_baseline leg")
     ap.add_argument("--case", default=None, metavar="FAMILY:T[:H[:QUANT[:KERNEL]]]",
                     help="run one workload --steps times without timing (for profilers), e.g. decode:128 or "
                          "bandwidth:1024:7168:none:stream")
@@ -328,14 +596,20 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import moe_finalize_residual_gb300 as mfr
+    from moe_finalize_residual_gb300.shard import token_range
     peak, peak_kind = peaks()
 
-    # ---------------- headline: T=128 decode, rotating input sets > 3x L2 -----------------------
+    # ---------------- headline: T=128 decode per GPU, rotating input sets > 3x L2 ------------------
+    # Weak scaling: the global batch is HEADLINE_T tokens per rank; rank r finalizes its token range
+    # of it (the tokens are independent, so no collective is involved) and draws its inputs from seeds
+    # offset by the range's first token.
+    tok0, tok1 = token_range(HEADLINE_T * world, rank, world)
+    assert tok1 - tok0 == HEADLINE_T
     one = synth.make_case("probe", T=HEADLINE_T, device=dev, **HEADLINE)
     bytes_call = algorithmic_bytes(one)
     del one
     nsets = max(2, -(-3 * L2_BYTES // bytes_call))
-    sets = make_sets(HEADLINE_T, nsets, dev)
+    sets = make_sets(HEADLINE_T, nsets, dev, tok0=tok0)
     outs = [alloc_outs(mfr, c)[0] for c in sets]
     calls = [finalize_fn(mfr, c, o) for c, o in zip(sets, outs)]
     plan = mfr.moe_finalize_plan([mfr.Partial(sets[0].gemm2[r], sets[0].perm[r], sets[0].scale[r], sets[0].shared[r])
@@ -344,291 +618,68 @@ def main():
     for _ in range(args.warmup):
         g.replay()
     torch.cuda.synchronize()
-    def timed_region():
-        """The K timed steps between barriers, clocks sampled meanwhile: (total ms, median µs per launch,
-        wall s, clock summary), the times the maximum over ranks."""
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        with ClockSampler(local) as clk:
-            t0 = time.perf_counter()
-            start = torch.cuda.Event(enable_timing=True)
-            stop = torch.cuda.Event(enable_timing=True)
-            start.record()
-            for a, b in evs:
-                a.record()
-                g.replay()
-                b.record()
-            stop.record()
-            torch.cuda.synchronize()
-            wall = time.perf_counter() - t0
-        if world > 1:
-            dist.barrier()
-        total_ms = start.elapsed_time(stop)
-        med = statistics.median([a.elapsed_time(b) * 1000.0 / GRAPH_LAUNCHES for a, b in evs])
-        if world > 1:
-            t = torch.tensor([total_ms, med], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms, med = float(t[0]), float(t[1])
-        return total_ms, med, wall, clk.summary()
 
-    def throttled(c):
-        """A throttle reason that invalidates a timing, or SM clocks well below their maximum with none."""
-        bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"} & set(c["reasons"])
-        low = c["sm_mhz"] is not None and c["sm_max_mhz"] and c["sm_mhz"] < 0.85 * c["sm_max_mhz"] and not c["reasons"]
-        return bool(bad) or bool(low)
-
-    total_ms, med_us, wall, clocks = timed_region()
+    total_ms, med_us, wall, clocks = headline_region(g, args.steps, world, dev, local)
     remeasured = None
     flag = torch.tensor([1.0 if throttled(clocks) else 0.0], device=dev)
     if world > 1:
         dist.all_reduce(flag, op=dist.ReduceOp.MAX)
     if flag.item() > 0:  # measured once more; the first figures are kept beside it
         remeasured = {"first_median_us": round(med_us, 3), "first_clocks": clocks}
-        total_ms, med_us, wall, clocks = timed_region()
+        total_ms, med_us, wall, clocks = headline_region(g, args.steps, world, dev, local)
     achieved = bytes_call / (med_us * 1e-6) / 1e9
     del g
 
     extras = {}
-    if rank == 0 and not args.no_extras:
-        # ---------------- the headline again with the early routing read (MFR_FLAG_ROUTING_READY) ----------
-        # Safe here and in a MoE layer: the routing is written long before the GEMM that precedes the
-        # finalize, and back-to-back finalize launches do not write it.  Same rotating input sets.
-        calls_rr = [finalize_fn(mfr, c, o, routing_ready=True) for c, o in zip(sets, outs)]
-        grr = capture_graph(lambda i: calls_rr[i % nsets]())
-        rr_us, _ = time_graph(grr, 200, 20)
-        extras["headline_routing_ready"] = {"us": round(rr_us, 3),
-                                            "gbs": round(bytes_call / (rr_us * 1e-6) / 1e9, 1),
-                                            "frac": round(bytes_call / (rr_us * 1e-6) / 1e9 / peak, 4)}
-        del grr, calls_rr
-        # ---------------- token sweep, L2-warm (the pages' setting), and launch floors -------------
-        sweep = []
-        for T in (1, 4, 16, 32, 64, 128):
-            c = make_sets(T, 1, dev)[0]
-            o = alloc_outs(mfr, c)[0]
-            fn = finalize_fn(mfr, c, o)
-            gg = capture_graph(lambda i: fn())
-            us, _ = time_graph(gg, 50, 5)
-            fn_rr = finalize_fn(mfr, c, o, routing_ready=True)
-            gr = capture_graph(lambda i: fn_rr())
-            us_rr, _ = time_graph(gr, 50, 5)
-            p = mfr.moe_finalize_plan([mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r])
-                                       for r in range(c.R)], c.residual, c.gamma)
-            sweep.append({"T": T, "us": round(us, 3), "us_routing_ready": round(us_rr, 3), "kernel": p["kernel"],
-                          "cluster": p["cluster"], "grid": p["grid"],
-                          "gbs_l2_warm": round(algorithmic_bytes(c) / (us * 1e-6) / 1e9, 1)})
-            del gg, gr, c, o
-        gf = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=True))
-        floor_pdl, _ = time_graph(gf, 50, 5)
-        gf2 = capture_graph(lambda i: mfr.moe_finalize_empty_launch(pdl=False))
-        floor_nopdl, _ = time_graph(gf2, 50, 5)
-        # the dependent index -> row -> store chain alone (20 rows, one per launch: L2-warm like the sweep)
-        rows = torch.zeros(1024, 6144, dtype=torch.bfloat16, device=dev)
-        gidx = torch.randint(0, rows.shape[0], (GRAPH_LAUNCHES, 1), dtype=torch.int32, device=dev)
-        gout = torch.empty(512, dtype=torch.uint8, device=dev)
-        gf3 = capture_graph(lambda i: mfr.moe_finalize_gather_floor_launch(gidx[i], rows, gout, pdl=True))
-        floor_gather, _ = time_graph(gf3, 50, 5)
-        del gf, gf2, gf3, rows
-        for s in sweep:
-            s["x_floor"] = round(s["us"] / floor_pdl, 2)
-            s["x_gather_floor"] = round(s["us"] / floor_gather, 2)
-        extras["sweep_l2_warm"] = sweep
-        extras["launch_floor_us"] = {"pdl": round(floor_pdl, 3), "no_pdl": round(floor_nopdl, 3),
-                                     "gather_chain_pdl": round(floor_gather, 3)}
-        del sets, outs, calls
-        torch.cuda.empty_cache()
+    if world == 1 and not args.no_extras:
+        extras.update(extra_sweep(mfr, dev, peak, sets, outs, nsets, bytes_call))
+    del sets, outs, calls
+    torch.cuda.empty_cache()
+    if world == 1 and not args.no_extras:
+        extras.update(extra_unfused(mfr, dev))
+        extras.update(extra_configs(mfr, dev, peak))
 
-        # ---------------- finalize-only, and fused vs unfused (finalize, then residual + RMSNorm) ----
-        # L2-warm graphs of 20 launches, the pages' setting.  The unfused pair's second launch is this
-        # library's fused call on one partial whose route is masked and whose shared row is the first
-        # launch's output S, with factor 1: it reads S, the residual and gamma and writes residual_out
-        # and norm_out, the work of a separate residual-RMSNorm kernel; its outputs are checked equal
-        # to the fused call's.
-        fin = []
-        for (H, E, K, R, shared, T) in ((6144, 256, 8, 4, True, 1), (6144, 256, 8, 4, True, 16),
-                                        (6144, 256, 8, 4, True, 128), (2048, 512, 22, 1, False, 16),
-                                        (3584, 896, 16, 1, False, 16), (4096, 512, 32, 1, False, 16),
-                                        (4096, 512, 32, 1, False, 128)):
-            c = synth.make_case("fin", T=T, H=H, E=E, K=K, R=R, rsf=2.5, shared=shared, device=dev,
-                                scale_dtype=torch.float32 if R == 1 else torch.bfloat16, seed_base=500_000)
-            parts = [mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r]) for r in range(c.R)]
-            o = alloc_outs(mfr, c)[0]
-            s_out = torch.empty_like(c.residual)
-            masked = torch.full((T, 1), -1, dtype=torch.int32, device=dev)
-            second = [mfr.Partial(c.gemm2[0][:1], masked, None, s_out)]
-            ro2, no2 = torch.empty_like(c.residual), torch.empty_like(c.residual)
-
-            def fused(i):
-                mfr.moe_finalize_fused(parts, c.residual, c.gamma, routed_scaling_factor=c.rsf, eps=c.eps,
-                                       residual_out=o[0], norm_out=o[1], check=False)
-
-            def fin_only(i):
-                mfr.moe_finalize_routed(parts, routed_scaling_factor=c.rsf, out=s_out, check=False)
-
-            def unfused(i):
-                fin_only(i)
-                mfr.moe_finalize_fused(second, c.residual, c.gamma, routed_scaling_factor=1.0, eps=c.eps,
-                                       residual_out=ro2, norm_out=no2, check=False)
-            res = {}
-            for name, fn in (("fused_us", fused), ("finalize_only_us", fin_only), ("unfused_pair_us", unfused)):
-                gg = capture_graph(fn)
-                res[name], _ = time_graph(gg, 50, 5)
-                del gg
-            torch.cuda.synchronize()
-            def ordinal(x):  # 16-bit float bit patterns as an ordered integer line (+0 and -0 equal)
-                b = x.view(torch.int16).to(torch.int32)
-                return torch.where(b < 0, -(b & 0x7FFF), b)
-            same = bool(torch.equal(o[0], ro2))
-            norm_ulp = int((ordinal(o[1]) - ordinal(no2)).abs().max())
-            fb = algorithmic_bytes(c, finalize_only=True)
-            fin.append({"H": H, "K": K, "R": R, "T": T, **{k: round(v, 3) for k, v in res.items()},
-                        "finalize_only_gbs_l2_warm": round(fb / (res["finalize_only_us"] * 1e-6) / 1e9, 1),
-                        "unfused_over_fused": round(res["unfused_pair_us"] / res["fused_us"], 3),
-                        "unfused_residual_out_equal": same, "unfused_norm_out_max_ulp": norm_ulp})
-            del c, parts, o, s_out, second, ro2, no2
-        extras["finalize_only_and_unfused_l2_warm"] = fin
-        torch.cuda.empty_cache()
-
-        # ---------------- every case of the tiny, masked and high-top-k workloads (L2-warm, like the
-        # pages' latency tables) and the bandwidth workload's H x T grid (inputs larger than L2) ----------
-        t_cfg = time.perf_counter()
-        rows_cfg = []
-        for fam in ("tiny", "masked", "highk", "bandwidth"):
-            for c in synth.config_cases(fam, device=dev):
-                o = alloc_outs(mfr, c)[0]
-                fn = finalize_fn(mfr, c, o)
-                big = fam == "bandwidth"
-                gg = capture_graph(lambda i: fn(), n=4 if big else GRAPH_LAUNCHES)
-                us, _ = time_graph(gg, 5 if big else 30, 2 if big else 3, launches=4 if big else GRAPH_LAUNCHES)
-                p = mfr.moe_finalize_plan([mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r])
-                                           for r in range(c.R)], c.residual, c.gamma)
-                b = algorithmic_bytes(c)
-                row = {"family": fam, "T": c.T, "H": c.H, "K": c.K, "R": c.R,
-                       "act": str(c.act_dtype).replace("torch.", ""),
-                       "scale": str(c.scale_dtype).replace("torch.", ""), "kernel": p["kernel"], "us": round(us, 3),
-                       "gbs": round(b / (us * 1e-6) / 1e9, 1), "l2": "inputs > L2" if big else "warm"}
-                if big:
-                    row["frac"] = round(b / (us * 1e-6) / 1e9 / peak, 3)
-                rows_cfg.append(row)
-                del gg, o
-                if big:  # the quantised outputs of the bandwidth workload, at every size
-                    for quant, lay in (("fp8", "row_major"), ("nvfp4", "row_major"), ("nvfp4", "swizzled_128x4")):
-                        oq, qs = alloc_outs(mfr, c, quant, lay)
-                        fq = finalize_fn(mfr, c, oq, quant, qs, lay)
-                        gq = capture_graph(lambda i: fq(), n=4)
-                        uq, _ = time_graph(gq, 5, 2, launches=4)
-                        bq = algorithmic_bytes(c, quant)
-                        rows_cfg.append({**row, "out": quant if quant == "fp8" else f"nvfp4-{lay}", "us": round(uq, 3),
-                                         "gbs": round(bq / (uq * 1e-6) / 1e9, 1),
-                                         "frac": round(bq / (uq * 1e-6) / 1e9 / peak, 3)})
-                        del gq, oq
-                del c
-            torch.cuda.empty_cache()
-        extras["configs"] = rows_cfg
-        extras["configs_wall_s"] = round(time.perf_counter() - t_cfg, 1)
-
-        # ---------------- bandwidth regime: H7168, T16384, R4, top-8 (inputs >> L2) ----------------
-        bw = []
-        c = synth.make_case("bandwidth-H7168-T16384", T=16384, H=7168, device=dev,
-                            **{k: v for k, v in synth.CONFIGS["bandwidth"].items() if k != "Ts"})
-        for quant, lay in (("none", "row_major"), ("fp8", "row_major"), ("nvfp4", "row_major"),
-                           ("nvfp4", "swizzled_128x4")):
-            o, qs = alloc_outs(mfr, c, quant, lay)
-            fn = finalize_fn(mfr, c, o, quant, qs, lay)
-            gg = capture_graph(lambda i: fn(), n=4)
-            us, _ = time_graph(gg, 10, 2, launches=4)
-            b = algorithmic_bytes(c, quant)
-            bw.append({"out": quant if quant != "nvfp4" else f"nvfp4-{lay}", "us": round(us, 1),
-                       "gb": round(b / 1e9, 3), "gbs": round(b / (us * 1e-6) / 1e9, 1),
-                       "frac": round(b / (us * 1e-6) / 1e9 / peak, 3)})
-            del gg, o
-        extras["bandwidth_H7168_T16384"] = bw
-        del c
-        torch.cuda.empty_cache()
-
-        # ---------------- end to end through the public API with host buffers ---------------------
-        # Every input of a step sits in one pinned host buffer and the device tensors are views of one
-        # device buffer (256-byte aligned slices), so a step is one host-to-device copy, the fused call
-        # and one device-to-host copy of residual_out and norm_out.
-        c = make_sets(HEADLINE_T, 1, dev)[0]
-        inputs = [*c.gemm2, *c.perm, *c.scale, *c.shared, c.residual, c.gamma]
-        sizes = [-(-t.numel() * t.element_size() // 256) * 256 for t in inputs]
-        host_in = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
-        dev_in = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
-        views, off = [], 0
-        for t, n in zip(inputs, sizes):
-            nb = t.numel() * t.element_size()
-            host_in[off:off + nb].view(t.dtype).view(t.shape).copy_(t.cpu())
-            views.append(dev_in[off:off + nb].view(t.dtype).view(t.shape))
-            off += n
-        R = c.R
-        g2, pm, sc, sh = views[:R], views[R:2 * R], views[2 * R:3 * R], views[3 * R:4 * R]
-        res_v, gam_v = views[4 * R], views[4 * R + 1]
-        parts_e2e = [mfr.Partial(g2[r], pm[r], sc[r], sh[r]) for r in range(R)]
-        out_bytes = c.residual.numel() * 2
-        dev_out = torch.empty(2 * out_bytes, dtype=torch.uint8, device=dev)
-        host_out = torch.empty(2 * out_bytes, dtype=torch.uint8).pin_memory()
-        ro_v = dev_out[:out_bytes].view(c.residual.dtype).view(c.residual.shape)
-        no_v = dev_out[out_bytes:].view(c.residual.dtype).view(c.residual.shape)
-        h2d = sum(t.numel() * t.element_size() for t in inputs)
-        d2h = 2 * out_bytes
-
-        # (splitting the input copy over 2-8 streams measured no faster: the host link is the limit)
-        def e2e_step():
-            dev_in.copy_(host_in, non_blocking=True)
-            mfr.moe_finalize_fused(parts_e2e, res_v, gam_v, routed_scaling_factor=c.rsf, eps=c.eps,
-                                   residual_out=ro_v, norm_out=no_v)
-            host_out.copy_(dev_out, non_blocking=True)
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        n_e2e = 50
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(n_e2e):
-            e2e_step()
-        b.record()
-        torch.cuda.synchronize()
-        e2e_us = a.elapsed_time(b) * 1000.0 / n_e2e
-        # the host copy of the result equals the same call on the original device tensors
-        ref_ro, ref_no, _, _ = mfr.moe_finalize_fused(
-            [mfr.Partial(c.gemm2[r], c.perm[r], c.scale[r], c.shared[r]) for r in range(R)], c.residual, c.gamma,
-            routed_scaling_factor=c.rsf, eps=c.eps)
-        torch.cuda.synchronize()
-        same = bool(torch.equal(host_out[:out_bytes], ref_ro.view(torch.uint8).reshape(-1).cpu()) and
-                    torch.equal(host_out[out_bytes:], ref_no.view(torch.uint8).reshape(-1).cpu()))
-        extras["e2e"] = {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                         "d2h_bytes_per_step": int(d2h), "copies_per_step": 2,
-                         "h2d_gbs": round(h2d / (e2e_us * 1e-6) / 1e9, 1),
-                         "result_equals_device_resident_call": same}
-        extras["cpu_baseline"] = cpu_baseline(c)
-        del c
+    # ---------------- end to end through the public API, every rank; the slowest decides ------------
+    e2e, c = e2e_headline(mfr, dev, tok0)
+    if world > 1:
+        t = torch.tensor([e2e["value"]], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["value"] = float(t[0])
+    e2e["value"] = round(e2e["value"], 2)
+    cpu = cpu_baseline(c, args.cpu_budget) if (rank == 0 and world == 1) else None
+    del c
 
     if rank == 0:
+        if args.extras_out:
+            os.makedirs(os.path.dirname(os.path.abspath(args.extras_out)), exist_ok=True)
+            with open(args.extras_out, "w") as f:
+                json.dump({**extras, "e2e": e2e, "cpu_baseline": cpu}, f, indent=1)
         line = {
             "metric": METRIC, "value": round(med_us, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
             "config": {"workload": f"decode H6144 E256 top-8 R4 shared rsf2.5 bf16, T={HEADLINE_T}",
-                       "global_batch": HEADLINE_T * world, "per_gpu_tokens": HEADLINE_T, "hidden": 6144,
-                       "top_k": 8, "partials": 4, "step": f"one CUDA-graph replay of {GRAPH_LAUNCHES} launches (PDL)",
-                       "l2": f"inputs larger than L2: {nsets} rotating input sets, {nsets * bytes_call / 1e6:.0f} MB",
-                       "kernel": plan["kernel"], "cluster": plan["cluster"], "grid": plan["grid"],
-                       "parallelism": f"dp{world} (token shards, no collective)"},
-            "mean_us": round(total_ms * 1000.0 / (args.steps * GRAPH_LAUNCHES), 3),
-            "tokens_per_s": round(HEADLINE_T * world / (med_us * 1e-6)),
+                       "global_batch": HEADLINE_T * world,
+                       "step": f"graph of {GRAPH_LAUNCHES} PDL launches",
+                       "l2": f"inputs > L2: {nsets} rotating sets, {nsets * bytes_call / 1e6:.0f} MB",
+                       "kernel": plan["kernel"], "parallelism": f"dp{world}, no collective"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic_for(f"{plan['kernel']}_decode_T128"),
-                         "peak_kind": f"of {peak_kind}", "algorithmic_bytes_per_launch": bytes_call},
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": bytes_call},
+            "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
             "gpu_launches": args.steps * GRAPH_LAUNCHES,
-            "clocks": clocks,
+            "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
             "timed_wall_s": round(wall, 3),
         }
+        if cpu is not None:
+            line["cpu_baseline"] = {k: (round(v, 1) if isinstance(v, float) else v) for k, v in cpu.items()}
         if remeasured is not None:
-            line["remeasured_after_throttling"] = remeasured
-        line.update(extras)
-        print(json.dumps(line), flush=True)
+            line["remeasured_after_throttling"] = {"first_median_us": remeasured["first_median_us"],
+                                                   "first_reasons": remeasured["first_clocks"]["reasons"]}
+        summ = summary_of(extras)
+        if summ:
+            line["summary"] = summ
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

@@ -97,7 +97,14 @@ enum {
    * its peers send, so every wait on it runs out after its limit (about 2 s) and is counted by
    * moe_finalize_read_timeouts.  The sums have all landed by then, so the outputs are still complete.
    * It has no effect on plans with one CTA per token or on the stream kernel.  Not for production use. */
-  MFR_FLAG_TEST_EXCHANGE_TIMEOUT = 1u << 30
+  MFR_FLAG_TEST_EXCHANGE_TIMEOUT = 1u << 30,
+  /* Test hook for failure detection: the stream kernel's end-of-token barrier (where a group's warps
+   * meet to add their sums of squares) expects one arrival more than its warps give, so every wait on
+   * it runs out after its limit (about 2 s), is counted by moe_finalize_read_timeouts, and the kernel
+   * returns early: tokens past each group's first are then not written, and norm_out and the quantised
+   * output of the first are not written either.  No effect on the cluster kernel or in finalize-only
+   * mode.  Not for production use. */
+  MFR_FLAG_TEST_STREAM_TIMEOUT = 1u << 29
 };
 
 /* Status codes. */
@@ -164,8 +171,10 @@ typedef struct {
  * Required: partials[r].gemm2_out and perm_idx for every r, and at least one of residual_out,
  * norm_out, quant_out, finalize_out.  residual and gamma are required unless finalize_out is the
  * only output (finalize-only mode: no residual add, RMSNorm or quantisation is done and neither is
- * read); gamma is needed also when norm_out is NULL, since the RMS feeds the quantisation.  Inputs
- * and outputs must not overlap. */
+ * read); gamma is needed also when norm_out is NULL, since the RMS feeds the quantisation.
+ * residual_out may be residual itself (the in-place residual update: each element of residual is
+ * read by the thread that later writes that element of residual_out).  No other input may overlap an
+ * output, and outputs must not overlap each other. */
 int moe_finalize_fused(const mfr_args* args, struct CUstream_st* stream);
 
 /* The geometry moe_finalize_fused would use for these arguments on the current device (validates
@@ -176,13 +185,16 @@ int moe_finalize_plan(const mfr_args* args, mfr_plan* plan);
  * scale buffer must be sized for the SWIZZLED_128x4 layout; T*H/16 is too small).  <0 on bad input. */
 int64_t moe_finalize_sf_bytes(int32_t T, int32_t H, int32_t sf_layout);
 
-/* Size in bytes of quant_out for T x H: T*H (FP8), T*H/2 (NVFP4), 0 (none).  <0 on bad input. */
+/* Size in bytes of quant_out for T x H: T*H (FP8, one E4M3 byte per element), T*H/2 (NVFP4, two E2M1
+ * codes per byte), 0 (none) -- the FP8 and NVFP4 quantised outputs of flashinfer PR #3385, Description.
+ * <0 on bad input. */
 int64_t moe_finalize_quant_bytes(int32_t T, int32_t H, int32_t quant_mode);
 
-/* Static text for a status code. */
+/* Static text for a status code (no counterpart on the pages). */
 const char* moe_finalize_status_string(int status);
 
-/* Message describing the last error returned to the calling thread ("" if none). */
+/* Message describing the last error returned to the calling thread ("" if none; no counterpart on
+ * the pages). */
 const char* moe_finalize_last_error(void);
 
 /* Measurement aid (no counterpart on the pages): enqueue one empty kernel launched the same way as

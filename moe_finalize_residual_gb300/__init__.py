@@ -27,6 +27,7 @@ __all__ = [
     "Partial", "moe_finalize_fused", "moe_finalize_routed", "moe_finalize_plan", "moe_finalize_sf_bytes", "moe_finalize_quant_bytes",
     "moe_finalize_empty_launch", "moe_finalize_gather_floor_launch", "moe_finalize_read_timeouts", "moe_finalize_abi_version", "library_path",
     "QUANT", "SF_LAYOUT", "KERNEL", "MFR_FLAG_PDL", "MFR_FLAG_ROUTING_READY", "MFR_FLAG_TEST_EXCHANGE_TIMEOUT",
+    "MFR_FLAG_TEST_STREAM_TIMEOUT",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -39,6 +40,7 @@ SF_LAYOUT = {"row_major": 0, "swizzled_128x4": 1}
 KERNEL = {"auto": 0, "cluster": 1, "stream": 2}
 MFR_FLAG_PDL, MFR_FLAG_ROUTING_READY = 1, 2
 MFR_FLAG_TEST_EXCHANGE_TIMEOUT = 1 << 30  # test hook: every cluster exchange wait runs out (see the C header)
+MFR_FLAG_TEST_STREAM_TIMEOUT = 1 << 29    # test hook: every stream end-of-token wait runs out (see the C header)
 STATUS = {0: "MFR_OK", -1: "MFR_ERR_INVALID_ARG", -2: "MFR_ERR_UNSUPPORTED", -3: "MFR_ERR_CUDA"}
 
 
@@ -252,7 +254,9 @@ def moe_finalize_fused(partials: Sequence[Partial], residual: torch.Tensor, gamm
         if quant_out is None:
             quant_out = torch.empty(int(moe_finalize_quant_bytes(T, H, qm)), dtype=torch.uint8, device=dev)
         if qm == QUANT["nvfp4"] and sf_out is None:
-            sf_out = torch.empty(int(moe_finalize_sf_bytes(T, H, sf_layout)), dtype=torch.uint8, device=dev)
+            # zero-filled: the kernel writes no padding bytes of the 128x4 layout, and a block-scaled GEMM
+            # reading the padded tile then sees zero scales, not stale memory
+            sf_out = torch.zeros(int(moe_finalize_sf_bytes(T, H, sf_layout)), dtype=torch.uint8, device=dev)
     else:
         quant_scale = None
     flags = (MFR_FLAG_PDL if pdl else 0) | (MFR_FLAG_ROUTING_READY if routing_ready else 0) | int(extra_flags)

@@ -84,7 +84,8 @@ int validate(const mfr_args* a) {
       return fail(MFR_ERR_UNSUPPORTED, "sf_layout %d: only ROW_MAJOR and SWIZZLED_128x4", a->sf_layout);
     if (a->H % 16 != 0) return fail(MFR_ERR_INVALID_ARG, "NVFP4 needs H %% 16 == 0 (H = %d)", a->H);
   }
-  if (a->flags & ~static_cast<uint32_t>(MFR_FLAG_PDL | MFR_FLAG_ROUTING_READY | MFR_FLAG_TEST_EXCHANGE_TIMEOUT))
+  if (a->flags & ~static_cast<uint32_t>(MFR_FLAG_PDL | MFR_FLAG_ROUTING_READY | MFR_FLAG_TEST_EXCHANGE_TIMEOUT |
+                                        MFR_FLAG_TEST_STREAM_TIMEOUT))
     return fail(MFR_ERR_INVALID_ARG, "unknown flag bits 0x%x", a->flags);
   if (a->kernel < MFR_KERNEL_AUTO || a->kernel > MFR_KERNEL_STREAM)
     return fail(MFR_ERR_INVALID_ARG, "kernel %d unknown", a->kernel);
@@ -160,6 +161,7 @@ void fill_params(const mfr_args* a, KParams* p) {
   p->routing_early = (p->pdl && (a->flags & MFR_FLAG_ROUTING_READY)) ? 1 : 0;
   p->rsf = a->routed_scaling_factor;
   p->eps = a->eps;
+  p->test_token_bar_extra = (a->flags & MFR_FLAG_TEST_STREAM_TIMEOUT) ? 1u : 0u;
 }
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }

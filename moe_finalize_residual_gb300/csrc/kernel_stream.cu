@@ -190,11 +190,12 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 1) stream_finalize_kernel(c
       mbar_init(rfull0 + 8u * i, 1);
       mbar_init(rempty0 + 8u * i, static_cast<uint32_t>(p.split ? G * NCW : NCW));
     }
+    // (the failure-detection test hook adds an arrival that never comes, so every wait on these runs out)
     if (p.split) {  // all groups work on every token: one reduction barrier pair for the CTA
-      mbar_init(cbar0, static_cast<uint32_t>(G * NCW));
-      mbar_init(cbar0 + 8u, static_cast<uint32_t>(G * NCW));
+      mbar_init(cbar0, static_cast<uint32_t>(G * NCW) + p.test_token_bar_extra);
+      mbar_init(cbar0 + 8u, static_cast<uint32_t>(G * NCW) + p.test_token_bar_extra);
     } else {
-      for (int i = 0; i < 2 * G; ++i) mbar_init(cbar0 + 8u * i, static_cast<uint32_t>(NCW));
+      for (int i = 0; i < 2 * G; ++i) mbar_init(cbar0 + 8u * i, static_cast<uint32_t>(NCW) + p.test_token_bar_extra);
     }
     *abort_flag = 0;
     fence_mbar_init();

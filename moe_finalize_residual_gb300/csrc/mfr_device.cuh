@@ -71,6 +71,8 @@ struct KParams {
   int32_t split;          // stream kernel: groups split each token's hidden passes (else the tokens)
   int32_t ring_bytes;     // bytes of one row-list entry
   int32_t off_bar, off_stage, off_ring, off_stash, off_sred;
+  uint32_t test_token_bar_extra;  // stream kernel: arrivals the end-of-token barrier expects beyond its
+                                  // warps' (1 only under the failure-detection test hook)
 };
 
 // ------------------------------------------------------------------------------------------------

@@ -104,7 +104,7 @@ def _raw_args(mfr, **over):
 
 BAD = [
     dict(H=12), dict(H=0), dict(H=65536), dict(K=0), dict(K=65), dict(R=0), dict(R=9), dict(T=-1),
-    dict(act_dtype=2), dict(scale_dtype=7), dict(quant_mode=3), dict(flags=8), dict(flags=1 | (1 << 29)),
+    dict(act_dtype=2), dict(scale_dtype=7), dict(quant_mode=3), dict(flags=8), dict(flags=1 | (1 << 28)),
     dict(kernel=3),
     dict(residual=None), dict(gamma=None), dict(residual=0xB00008), dict(norm_out=0xE00004),
     dict(residual_out=None, norm_out=None),
@@ -181,8 +181,9 @@ def test_valid_call_without_gpu_reports_cuda_error(mfr):
 def test_timeout_test_flag_passes_validation(mfr):
     """The failure-detection test hook is a known flag bit: validation accepts it (the call then reaches
     the CUDA runtime, which reports no device here)."""
-    a, keep = _raw_args(mfr, flags=1 | mfr.MFR_FLAG_TEST_EXCHANGE_TIMEOUT)
-    assert mfr.raw_library().moe_finalize_fused(ctypes.byref(a), None) == -3
+    for flag in (mfr.MFR_FLAG_TEST_EXCHANGE_TIMEOUT, mfr.MFR_FLAG_TEST_STREAM_TIMEOUT):
+        a, keep = _raw_args(mfr, flags=1 | flag)
+        assert mfr.raw_library().moe_finalize_fused(ctypes.byref(a), None) == -3
 
 
 def test_import_fails_loudly_without_library(tmp_path):

@@ -47,17 +47,15 @@ def test_decode(T, kernel):
 
 
 def _masked_cases():
+    """The whole masked workload: T x top-k x activation type x partials x scale type (flashinfer PR #6631,
+    Test changes: top_k 6/8/10, a quarter of the routes -1, fp16 and bf16, TP2 and TP4)."""
     out = []
-    for case_T in (1, 16):
+    for case_T in synth.CONFIGS["masked"]["Ts"]:
         for K in (6, 8, 10):
             for act in (torch.float16, torch.bfloat16):
                 for R in (2, 4):
                     for sdt in (torch.float32, torch.bfloat16):
                         out.append((case_T, K, act, R, sdt))
-    for i, T in enumerate((64, 128)):
-        for K in (6, 8, 10):
-            out.append((T, K, (torch.float16, torch.bfloat16)[(K + i) % 2], (2, 4)[(K // 2 + i) % 2],
-                        (torch.float32, torch.bfloat16)[i]))
     return out
 
 
@@ -469,6 +467,75 @@ def test_exchange_wait_that_runs_out_is_counted():
     check_against_oracle(case, res)
     check_against_oracle(case, run(g, kernel="cluster"))
     assert mfr.moe_finalize_read_timeouts() == 0
+
+
+def test_stream_wait_that_runs_out_is_counted():
+    """Failure detection in the stream kernel, on the GPU without a fault: the test hook makes the
+    end-of-token barrier of every group expect one arrival more than its warps give, so each wait on it
+    runs out after its limit (about 2 s), is counted, and the kernel returns early (the abort flag stops
+    the other warps; every thread waits for its own copies before it exits).  The context stays usable:
+    a normal call afterwards matches the oracle and counts nothing.  Both stream modes: groups splitting
+    one token's hidden dimension (at most one token per CTA) and groups streaming their own tokens."""
+    import moe_finalize_residual_gb300 as mfr
+    assert mfr.moe_finalize_read_timeouts() == 0
+    for T, H in ((4, 1024), (400, 256)):
+        case = synth.make_case("stream-timeout", T=T, H=H, K=8, R=2, E=64, rsf=2.5, shared=True)
+        g = on_gpu(case)
+        plan = mfr.moe_finalize_plan(partials_of(g), g.residual, g.gamma, kernel="stream")
+        assert plan["kernel"] == "stream", plan
+        t0 = time.monotonic()
+        res = run(g, kernel="stream", extra_flags=mfr.MFR_FLAG_TEST_STREAM_TIMEOUT)
+        elapsed = time.monotonic() - t0
+        assert res.guards_ok
+        assert mfr.moe_finalize_read_timeouts() > 0
+        assert 1.0 < elapsed < 60.0, elapsed
+        want = oracle.finalize(case)
+        if T <= 152:  # one token per CTA: residual_out is written before the token's barrier
+            assert np.array_equal(res.residual_out, want["residual_out"])
+        check_against_oracle(case, run(g, kernel="stream"), want)
+        assert mfr.moe_finalize_read_timeouts() == 0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("H,E,K,R,shared,T", [(6144, 256, 8, 4, True, 1), (6144, 256, 8, 4, True, 16),
+                                              (6144, 256, 8, 4, True, 128), (4096, 512, 32, 1, False, 16),
+                                              (7168, 256, 10, 2, False, 64)])
+def test_unfused_pair_matches_oracle(H, E, K, R, shared, T, kernel):
+    """The unfused pair the benchmark times against the fused call (flashinfer PR #6631, Description:
+    finalize, then a separate residual + RMSNorm kernel): finalize-only into S, then a second launch that
+    reads S as the only row of a one-partial call with its route masked and factor 1 -- the bytes of a
+    residual-RMSNorm kernel.  Both launches go out back to back with PDL; the pair must give the oracle's
+    residual_out bit for bit and its norm_out within 1 ulp."""
+    import moe_finalize_residual_gb300 as mfr
+    case = synth.make_case("unfused", T=T, H=H, E=E, K=K, R=R, rsf=2.5, shared=shared,
+                           scale_dtype=torch.float32 if R == 1 else torch.bfloat16, mask_quarter=not shared)
+    g = on_gpu(case)
+    s_out = torch.empty_like(g.residual)
+    mfr.moe_finalize_routed(partials_of(g), routed_scaling_factor=g.rsf, out=s_out, kernel=kernel)
+    masked = torch.full((T, 1), -1, dtype=torch.int32, device="cuda")
+    second = synth.Case("second", T, H, 1, 1, 1, g.act_dtype, None, 1.0, g.eps, [g.gemm2[0][:1]], [masked], [None],
+                        [s_out], [masked], g.residual, g.gamma)
+    res = run(second, kernel=kernel)
+    assert res.guards_ok
+    check_against_oracle(case, res)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("T", [1, 16, 128, 600])
+def test_residual_out_in_place(T, kernel):
+    """residual_out may be the residual tensor itself (the usual in-place residual update): every element
+    of residual is read by the same thread, before it writes that element of residual_out."""
+    import moe_finalize_residual_gb300 as mfr
+    case = synth.make_case("inplace", T=T, H=2048, K=8, R=2, E=64, rsf=2.5, shared=True)
+    want = oracle.finalize(case)
+    g = on_gpu(case)
+    res_buf = g.residual.clone()
+    norm = torch.empty_like(res_buf)
+    mfr.moe_finalize_fused(partials_of(g), res_buf, g.gamma, routed_scaling_factor=g.rsf, eps=g.eps,
+                           residual_out=res_buf, norm_out=norm, kernel=kernel)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(res_buf), want["residual_out"])
+    assert ulp_distance(bits16(norm), want["norm_out"]).max() <= 1
 
 
 # ------------------------------------------------------------------------------------------------------
