@@ -81,7 +81,9 @@ typedef enum {
 typedef enum {
   MFR_KERNEL_AUTO = 0,
   MFR_KERNEL_CLUSTER = 1, /* small batch: one thread-block cluster per token, hidden split over CTAs */
-  MFR_KERNEL_STREAM = 2   /* large batch: persistent CTAs, rows streamed by per-thread async copies */
+  MFR_KERNEL_STREAM = 2,  /* large batch: persistent CTAs, rows streamed by per-thread async copies */
+  MFR_KERNEL_BULK = 3     /* large batch: persistent CTAs, rows staged by bulk copies (cp.async.bulk)
+                             that a producer warp issues, several rows per mbarrier-counted stage     */
 } mfr_kernel;
 
 /* Flags. */
@@ -157,14 +159,15 @@ typedef struct {
 
 /* Launch geometry chosen for a call (for tests and benchmarks). */
 typedef struct {
-  int32_t kernel;     /* MFR_KERNEL_CLUSTER or MFR_KERNEL_STREAM                                     */
+  int32_t kernel;     /* MFR_KERNEL_CLUSTER, MFR_KERNEL_STREAM or MFR_KERNEL_BULK                    */
   int32_t grid;       /* CTAs launched                                                               */
   int32_t cluster;    /* CTAs per cluster (1 = no cluster)                                           */
   int32_t block;      /* threads per CTA                                                             */
   int32_t smem_bytes; /* dynamic shared memory per CTA                                               */
-  int32_t chunk;      /* stream kernel: hidden elements per pipeline stage; cluster kernel: hidden   */
+  int32_t chunk;      /* stream and bulk kernels: hidden elements per pass; cluster kernel: hidden   */
                       /* elements per chunk of a CTA                                                */
-  int32_t stages;     /* stream kernel: pipeline depth; cluster kernel: chunks per CTA               */
+  int32_t stages;     /* stream kernel: row slots per group; bulk kernel: stages (each of several    */
+                      /* rows); cluster kernel: chunks per CTA                                      */
 } mfr_plan;
 
 /* Enqueue the fused finalize.  Returns MFR_OK or a negative status (see above).

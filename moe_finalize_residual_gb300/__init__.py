@@ -37,7 +37,7 @@ MFR_BF16, MFR_FP16, MFR_FP32 = 0, 1, 2
 DTYPE = {torch.bfloat16: MFR_BF16, torch.float16: MFR_FP16, torch.float32: MFR_FP32}
 QUANT = {"none": 0, "fp8": 1, "nvfp4": 2}
 SF_LAYOUT = {"row_major": 0, "swizzled_128x4": 1}
-KERNEL = {"auto": 0, "cluster": 1, "stream": 2}
+KERNEL = {"auto": 0, "cluster": 1, "stream": 2, "bulk": 3}
 MFR_FLAG_PDL, MFR_FLAG_ROUTING_READY = 1, 2
 MFR_FLAG_TEST_EXCHANGE_TIMEOUT = 1 << 30  # test hook: every cluster exchange wait runs out (see the C header)
 MFR_FLAG_TEST_STREAM_TIMEOUT = 1 << 29    # test hook: every stream end-of-token wait runs out (see the C header)
@@ -305,7 +305,7 @@ def moe_finalize_plan(partials: Sequence[Partial], residual: torch.Tensor, gamma
     _check(_lib.moe_finalize_plan(ctypes.byref(a), ctypes.byref(plan)))
     del keep
     out = {n: getattr(plan, n) for n, _ in _CPlan._fields_}
-    out["kernel"] = {1: "cluster", 2: "stream"}.get(out["kernel"], "none")
+    out["kernel"] = {1: "cluster", 2: "stream", 3: "bulk"}.get(out["kernel"], "none")
     return out
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_finalize.so")
-SOURCES = ["api.cu", "kernel_cluster.cu", "kernel_stream.cu"]
+SOURCES = ["api.cu", "kernel_cluster.cu", "kernel_stream.cu", "kernel_bulk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

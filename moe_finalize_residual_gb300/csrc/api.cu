@@ -41,6 +41,7 @@ std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
 std::map<std::tuple<int, int, int, int, int>, int> g_cluster_ok;  // (dev, act, C, block, smem) -> clusters
 std::map<std::tuple<int, int, int, int, int>, int> g_stream_bps;  // (dev, act, groups, block, smem) -> blocks/SM
+std::map<std::tuple<int, int, int, int, int>, int> g_bulk_bps;    // (dev, act, columns, block, smem) -> blocks/SM
 
 int device_info(DeviceInfo* out, int* dev_out) {
   int dev = 0;
@@ -87,7 +88,7 @@ int validate(const mfr_args* a) {
   if (a->flags & ~static_cast<uint32_t>(MFR_FLAG_PDL | MFR_FLAG_ROUTING_READY | MFR_FLAG_TEST_EXCHANGE_TIMEOUT |
                                         MFR_FLAG_TEST_STREAM_TIMEOUT))
     return fail(MFR_ERR_INVALID_ARG, "unknown flag bits 0x%x", a->flags);
-  if (a->kernel < MFR_KERNEL_AUTO || a->kernel > MFR_KERNEL_STREAM)
+  if (a->kernel < MFR_KERNEL_AUTO || a->kernel > MFR_KERNEL_BULK)
     return fail(MFR_ERR_INVALID_ARG, "kernel %d unknown", a->kernel);
   if (a->T == 0) return MFR_OK;  // nothing to read or write
   if (a->partials == nullptr) return fail(MFR_ERR_INVALID_ARG, "partials is NULL");
@@ -354,6 +355,64 @@ bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, La
   return false;
 }
 
+// Bulk-copy kernel: persistent CTAs (one per SM) of a routing warp, a copy warp and kBulkComputeWarps
+// compute warps,
+// each CTA finalizing whole tokens in turn.  A pass covers the whole row when the compute threads can
+// hold it in kBulkMaxColumns 16-byte columns each, else the row is cut into equal passes (multiples of
+// 16 elements).  The ring takes stages of SR row slots: four stages, each with as many rows as shared
+// memory allows (at least one, at most 8), fewer stages only when even one row per stage does not fit.
+bool plan_bulk(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
+  const int nct = 32 * kBulkComputeWarps;
+  const int block = 64 + nct;  // a routing warp, a copy warp and the compute warps
+  const int max_pass = 8 * nct * kBulkMaxColumns;
+  const int npass = ceil_div(a->H, max_pass);
+  const int W = npass == 1 ? a->H : align_up(ceil_div(a->H, npass), 16);
+  const int Q = ceil_div(ceil_div(W, 8), nct);
+  const int slot_bytes = W * 2;
+  const int ring_bytes = align_up(16 + (p->nslots + 1) * 16, 16);  // the count, then the entries and the residual row
+  for (int nst = 4; nst >= 2; --nst) {
+    const int off_bar = 0;
+    const int bar_bytes = 8 * (2 * nst + 2 * 4 + 2) + 8;  // stages, lists, the token meeting; abort flag
+    const int off_ring = align_up(off_bar + bar_bytes, 16);
+    const int off_stash = align_up(off_ring + 4 * ring_bytes, 16);
+    const int off_sred = align_up(off_stash + a->H * 2, 16);
+    const int off_stage = align_up(off_sred + 2 * 32 * 4, 128);
+    const int room = d.smem_optin - off_stage;
+    const int sr = std::min(8, room / (nst * slot_bytes));
+    if (sr < 1) continue;
+    const int smem = off_stage + nst * sr * slot_bytes;
+    LaunchGeom geo{0, block, 1, smem, d.smem_optin};
+    const auto key = std::make_tuple(dev, a->act_dtype, Q, block, smem);
+    int bps;
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      auto it = g_bulk_bps.find(key);
+      bps = (it == g_bulk_bps.end()) ? -1 : it->second;
+    }
+    if (bps < 0) {
+      bps = bulk_kernel_blocks_per_sm(a->act_dtype, Q, geo);
+      std::lock_guard<std::mutex> lock(g_mu);
+      g_bulk_bps[key] = bps;
+    }
+    if (bps < 1) continue;
+    geo.grid = std::min(a->T, d.sms * bps);
+    p->chunk = W;
+    p->stages = nst;
+    p->stage_rows = sr;
+    p->stage_bytes = slot_bytes;
+    p->cols_per_thread = Q;
+    p->ring_bytes = ring_bytes;
+    p->off_bar = off_bar;
+    p->off_stage = off_stage;
+    p->off_ring = off_ring;
+    p->off_stash = off_stash;
+    p->off_sred = off_sred;
+    *g = geo;
+    return true;
+  }
+  return false;
+}
+
 int make_plan(const mfr_args* a, KParams* p, LaunchGeom* g, int* kernel) {
   int st = validate(a);
   if (st != MFR_OK) return st;
@@ -370,6 +429,14 @@ int make_plan(const mfr_args* a, KParams* p, LaunchGeom* g, int* kernel) {
   if (want_cluster && plan_cluster(a, d, dev, p, g)) {
     *kernel = MFR_KERNEL_CLUSTER;
     return MFR_OK;
+  }
+  if (a->kernel == MFR_KERNEL_BULK) {
+    if (plan_bulk(a, d, dev, p, g)) {
+      *kernel = MFR_KERNEL_BULK;
+      return MFR_OK;
+    }
+    return fail(MFR_ERR_UNSUPPORTED, "the bulk kernel does not fit T=%d H=%d K=%d R=%d in shared memory", a->T, a->H,
+                a->K, a->R);
   }
   if (a->kernel != MFR_KERNEL_CLUSTER && plan_stream(a, d, dev, p, g)) {
     *kernel = MFR_KERNEL_STREAM;
@@ -418,6 +485,7 @@ int moe_finalize_fused(const mfr_args* args, struct CUstream_st* stream) {
   int st = make_plan(args, &p, &g, &kernel);
   if (st != MFR_OK || args->T == 0) return st;
   cudaError_t e = (kernel == MFR_KERNEL_CLUSTER) ? launch_cluster_kernel(args->act_dtype, p, g, stream)
+                  : (kernel == MFR_KERNEL_BULK)  ? launch_bulk_kernel(args->act_dtype, p, g, stream)
                                                  : launch_stream_kernel(args->act_dtype, p, g, stream);
   if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   return MFR_OK;
@@ -435,8 +503,8 @@ int moe_finalize_plan(const mfr_args* args, mfr_plan* plan) {
   plan->cluster = g.cluster;
   plan->block = g.block;
   plan->smem_bytes = g.smem;
-  plan->chunk = kernel == MFR_KERNEL_STREAM ? p.chunk : p.slice_vec * 8;  // cluster: hidden elements per chunk
-  plan->stages = kernel == MFR_KERNEL_STREAM ? p.stages : p.nchunk;     // cluster: chunks per CTA
+  plan->chunk = kernel == MFR_KERNEL_CLUSTER ? p.slice_vec * 8 : p.chunk;  // cluster: hidden elements per chunk
+  plan->stages = kernel == MFR_KERNEL_CLUSTER ? p.nchunk : p.stages;       // cluster: chunks per CTA
   return MFR_OK;
 }
 
@@ -511,11 +579,12 @@ int moe_finalize_gather_floor_launch(const int32_t* idx, const void* rows, int64
 
 int moe_finalize_read_timeouts(uint32_t* count) {
   if (count == nullptr) return fail(MFR_ERR_INVALID_ARG, "count is NULL");
-  unsigned int c = 0, cc = 0;
+  unsigned int c = 0, cc = 0, cb = 0;
   cudaError_t e = read_and_reset_timeouts(&c);
   if (e == cudaSuccess) e = read_and_reset_cluster_timeouts(&cc);
+  if (e == cudaSuccess) e = read_and_reset_bulk_timeouts(&cb);
   if (e != cudaSuccess) return fail(MFR_ERR_CUDA, "reading the timeout counters: %s", cudaGetErrorString(e));
-  *count = c + cc;
+  *count = c + cc + cb;
   return MFR_OK;
 }
 

@@ -71,8 +71,11 @@ struct KParams {
   int32_t split;          // stream kernel: groups split each token's hidden passes (else the tokens)
   int32_t ring_bytes;     // bytes of one row-list entry
   int32_t off_bar, off_stage, off_ring, off_stash, off_sred;
-  uint32_t test_token_bar_extra;  // stream kernel: arrivals the end-of-token barrier expects beyond its
+  uint32_t test_token_bar_extra;  // stream kernels: arrivals the end-of-token barrier expects beyond their
                                   // warps' (1 only under the failure-detection test hook)
+  // bulk-copy kernel (also chunk = pass width, stages, stage_bytes = one row slot, ring_bytes, offsets)
+  int32_t stage_rows;       // rows per stage (one mbarrier per stage)
+  int32_t cols_per_thread;  // 16-byte columns per compute thread per pass (template parameter)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -147,6 +150,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The same test, but the thread may sleep (up to about `hint_ns`) until the phase completes instead of
+// returning at once: waiting warps then take no issue slots from the working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }

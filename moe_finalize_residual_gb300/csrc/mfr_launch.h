@@ -30,6 +30,12 @@ constexpr int kStreamColumns = MFR_STREAM_COLUMNS;  // 16-byte columns per compu
 static_assert(kStreamLists % kStreamGroups == 0, "a list slot must return to the group that used it");
 static_assert(kStreamGroups == 1 || kStreamGroups == 2, "the stream kernel is built for one or two groups");
 constexpr int kClusterMaxThreads = 512;             // R groups of SV threads
+// Bulk-copy streaming kernel: a routing warp, a copy warp and this many compute warps.
+#ifndef MFR_BULK_COMPUTE_WARPS
+#define MFR_BULK_COMPUTE_WARPS 14
+#endif
+constexpr int kBulkComputeWarps = MFR_BULK_COMPUTE_WARPS;
+constexpr int kBulkMaxColumns = 4;                  // 16-byte columns per compute thread per pass
 
 
 struct LaunchGeom {
@@ -49,7 +55,10 @@ int cluster_kernel_max_active_clusters(int act_dtype, int form, const LaunchGeom
 int cluster_kernel_blocks_per_sm(int act_dtype, int form, const LaunchGeom& g);
 cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
 int stream_kernel_blocks_per_sm(int act_dtype, int groups, const LaunchGeom& g);
+cudaError_t launch_bulk_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
+int bulk_kernel_blocks_per_sm(int act_dtype, int cols_per_thread, const LaunchGeom& g);
 cudaError_t read_and_reset_timeouts(unsigned int* count);
+cudaError_t read_and_reset_bulk_timeouts(unsigned int* count);
 cudaError_t read_and_reset_cluster_timeouts(unsigned int* count);
 
 }  // namespace mfr

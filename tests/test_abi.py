@@ -105,7 +105,7 @@ def _raw_args(mfr, **over):
 BAD = [
     dict(H=12), dict(H=0), dict(H=65536), dict(K=0), dict(K=65), dict(R=0), dict(R=9), dict(T=-1),
     dict(act_dtype=2), dict(scale_dtype=7), dict(quant_mode=3), dict(flags=8), dict(flags=1 | (1 << 28)),
-    dict(kernel=3),
+    dict(kernel=4), dict(kernel=-1),
     dict(residual=None), dict(gamma=None), dict(residual=0xB00008), dict(norm_out=0xE00004),
     dict(residual_out=None, norm_out=None),
     dict(residual_out=None, norm_out=None, finalize_out=0xD00008),  # misaligned finalize_out

@@ -17,7 +17,7 @@ from helpers import (CANARY, contraction_case, Guarded, nan16, as_f64, bits16, c
                      quant_scale_for, run, subcase, ulp_distance)
 
 pytestmark = pytest.mark.gpu
-KERNELS = ["cluster", "stream"]
+KERNELS = ["cluster", "stream", "bulk"]
 
 
 def on_gpu(case):
@@ -168,15 +168,18 @@ def test_bandwidth_sampled(T, H):
     toks = _sample_tokens(T)
     sub = subcase(case, toks)
     want = oracle.finalize(sub)
-    for kernel in ("auto", "stream"):
+    for kernel in ("auto", "stream", "bulk"):
         res = run(case, kernel=kernel)
         assert res.guards_ok
         check_against_oracle(sub, res, want, tokens=toks)
     # quantised variants at the same size; the global scale assumes |norm_out| <= 8, which holds for unit-
     # variance residuals with gamma near 1 (values beyond it saturate identically on both sides)
-    for quant, layout, qs in (("fp8", "row_major", 448.0 / 8), ("nvfp4", "row_major", 448.0 * 6 / 8),
-                              ("nvfp4", "swizzled_128x4", 448.0 * 6 / 8)):
-        res = run(case, kernel="auto", quant=quant, qscale=qs, sf_layout=layout)
+    for kernel, quant, layout, qs in (("auto", "fp8", "row_major", 448.0 / 8),
+                                      ("auto", "nvfp4", "row_major", 448.0 * 6 / 8),
+                                      ("auto", "nvfp4", "swizzled_128x4", 448.0 * 6 / 8),
+                                      ("bulk", "fp8", "row_major", 448.0 / 8),
+                                      ("bulk", "nvfp4", "swizzled_128x4", 448.0 * 6 / 8)):
+        res = run(case, kernel=kernel, quant=quant, qscale=qs, sf_layout=layout)
         assert res.guards_ok
         check_against_oracle(sub, res, want, tokens=toks)
         lay = oracle.SF_ROW_MAJOR if layout == "row_major" else oracle.SF_SWIZZLED_128x4
@@ -469,22 +472,24 @@ def test_exchange_wait_that_runs_out_is_counted():
     assert mfr.moe_finalize_read_timeouts() == 0
 
 
-def test_stream_wait_that_runs_out_is_counted():
-    """Failure detection in the stream kernel, on the GPU without a fault: the test hook makes the
-    end-of-token barrier of every group expect one arrival more than its warps give, so each wait on it
-    runs out after its limit (about 2 s), is counted, and the kernel returns early (the abort flag stops
-    the other warps; every thread waits for its own copies before it exits).  The context stays usable:
-    a normal call afterwards matches the oracle and counts nothing.  Both stream modes: groups splitting
-    one token's hidden dimension (at most one token per CTA) and groups streaming their own tokens."""
+@pytest.mark.parametrize("kernel", ["stream", "bulk"])
+def test_stream_wait_that_runs_out_is_counted(kernel):
+    """Failure detection in the streaming kernels, on the GPU without a fault: the test hook makes the
+    end-of-token barrier (where the compute warps meet to add their sums of squares) expect one arrival
+    more than its warps give, so each wait on it runs out after its limit (about 2 s), is counted, and
+    the kernel returns early (the abort flag stops the other warps; every copy in flight lands before the
+    CTA exits).  The context stays usable: a normal call afterwards matches the oracle and counts
+    nothing.  At most one token per CTA (groups splitting a token's hidden dimension in the stream
+    kernel) and several tokens per CTA."""
     import moe_finalize_residual_gb300 as mfr
     assert mfr.moe_finalize_read_timeouts() == 0
     for T, H in ((4, 1024), (400, 256)):
         case = synth.make_case("stream-timeout", T=T, H=H, K=8, R=2, E=64, rsf=2.5, shared=True)
         g = on_gpu(case)
-        plan = mfr.moe_finalize_plan(partials_of(g), g.residual, g.gamma, kernel="stream")
-        assert plan["kernel"] == "stream", plan
+        plan = mfr.moe_finalize_plan(partials_of(g), g.residual, g.gamma, kernel=kernel)
+        assert plan["kernel"] == kernel, plan
         t0 = time.monotonic()
-        res = run(g, kernel="stream", extra_flags=mfr.MFR_FLAG_TEST_STREAM_TIMEOUT)
+        res = run(g, kernel=kernel, extra_flags=mfr.MFR_FLAG_TEST_STREAM_TIMEOUT)
         elapsed = time.monotonic() - t0
         assert res.guards_ok
         assert mfr.moe_finalize_read_timeouts() > 0
@@ -492,7 +497,7 @@ def test_stream_wait_that_runs_out_is_counted():
         want = oracle.finalize(case)
         if T <= 152:  # one token per CTA: residual_out is written before the token's barrier
             assert np.array_equal(res.residual_out, want["residual_out"])
-        check_against_oracle(case, run(g, kernel="stream"), want)
+        check_against_oracle(case, run(g, kernel=kernel), want)
         assert mfr.moe_finalize_read_timeouts() == 0
 
 
