@@ -167,11 +167,18 @@ void fill_params(const mfr_args* a, KParams* p) {
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
-// Token count up to which the cluster kernel is chosen automatically (measured on GB300 at H=6144,
-// top-8, R=4: the cluster kernel is ahead up to 512 tokens, the stream kernel from about 1024), and
-// the cluster planner's targets (probe builds may override them).
-#ifndef MFR_CLUSTER_MAX_TOKENS
-#define MFR_CLUSTER_MAX_TOKENS 512
+// Automatic choice (measured on GB300, L2-cold): the bulk-copy kernel once every SM streams at least
+// kBulkMinTokensPerSm whole tokens and a row is at least kBulkMinHidden elements (bulk copies of 8 KB
+// and more), else the cluster kernel.  Decode rows (H=6144, top-8, R=4, shared rows): cluster ahead up
+// to 768 tokens (67.6 against 72.1 us), bulk from 1024 (84.4 against 87.0).  Bandwidth rows (H=7168, no
+// shared rows): bulk from 768 (72.8 against 74.0; T=1024 87.3 against 94.1).  H=2048: cluster ahead at
+// every size measured (T=2048: 61.2 against 87.4), the per-row work of 4 KB rows being too small for a
+// compute warp.  The cluster planner's targets follow (probe builds may override them).
+#ifndef MFR_BULK_MIN_TOKENS_PER_SM
+#define MFR_BULK_MIN_TOKENS_PER_SM 6
+#endif
+#ifndef MFR_BULK_MIN_HIDDEN
+#define MFR_BULK_MIN_HIDDEN 4096
 #endif
 #ifndef MFR_CLUSTER_BLOCK
 #define MFR_CLUSTER_BLOCK 512
@@ -182,7 +189,8 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 #ifndef MFR_CLUSTER_MAX_SIZE
 #define MFR_CLUSTER_MAX_SIZE 16
 #endif
-constexpr int kClusterMaxTokens = MFR_CLUSTER_MAX_TOKENS;
+constexpr int kBulkMinTokensPerSm = MFR_BULK_MIN_TOKENS_PER_SM;
+constexpr int kBulkMinHidden = MFR_BULK_MIN_HIDDEN;
 constexpr int kMaxCluster = MFR_CLUSTER_MAX_SIZE;
 
 // Cluster kernel: C CTAs per token, each covering NCH chunks of SV 16-byte vectors of the hidden row
@@ -424,27 +432,34 @@ int make_plan(const mfr_args* a, KParams* p, LaunchGeom* g, int* kernel) {
   int dev = 0;
   if ((st = device_info(&d, &dev)) != MFR_OK) return st;
   fill_params(a, p);
-  const bool want_cluster =
-      a->kernel == MFR_KERNEL_CLUSTER || (a->kernel == MFR_KERNEL_AUTO && a->T <= kClusterMaxTokens);
-  if (want_cluster && plan_cluster(a, d, dev, p, g)) {
+  const bool auto_bulk = static_cast<int64_t>(a->T) >= static_cast<int64_t>(kBulkMinTokensPerSm) * d.sms &&
+                         a->H >= kBulkMinHidden;
+  const int first = a->kernel != MFR_KERNEL_AUTO ? a->kernel : auto_bulk ? MFR_KERNEL_BULK : MFR_KERNEL_CLUSTER;
+  if (first == MFR_KERNEL_BULK && plan_bulk(a, d, dev, p, g)) {
+    *kernel = MFR_KERNEL_BULK;
+    return MFR_OK;
+  }
+  if (first == MFR_KERNEL_CLUSTER && plan_cluster(a, d, dev, p, g)) {
     *kernel = MFR_KERNEL_CLUSTER;
     return MFR_OK;
   }
-  if (a->kernel == MFR_KERNEL_BULK) {
-    if (plan_bulk(a, d, dev, p, g)) {
-      *kernel = MFR_KERNEL_BULK;
-      return MFR_OK;
-    }
-    return fail(MFR_ERR_UNSUPPORTED, "the bulk kernel does not fit T=%d H=%d K=%d R=%d in shared memory", a->T, a->H,
-                a->K, a->R);
-  }
-  if (a->kernel != MFR_KERNEL_CLUSTER && plan_stream(a, d, dev, p, g)) {
+  if (first == MFR_KERNEL_STREAM && plan_stream(a, d, dev, p, g)) {
     *kernel = MFR_KERNEL_STREAM;
     return MFR_OK;
   }
-  if (a->kernel == MFR_KERNEL_AUTO && plan_cluster(a, d, dev, p, g)) {
-    *kernel = MFR_KERNEL_CLUSTER;
-    return MFR_OK;
+  if (a->kernel == MFR_KERNEL_AUTO) {  // the other kernels, when the first choice does not fit
+    if (first != MFR_KERNEL_CLUSTER && plan_cluster(a, d, dev, p, g)) {
+      *kernel = MFR_KERNEL_CLUSTER;
+      return MFR_OK;
+    }
+    if (first != MFR_KERNEL_BULK && plan_bulk(a, d, dev, p, g)) {
+      *kernel = MFR_KERNEL_BULK;
+      return MFR_OK;
+    }
+    if (plan_stream(a, d, dev, p, g)) {
+      *kernel = MFR_KERNEL_STREAM;
+      return MFR_OK;
+    }
   }
   return fail(MFR_ERR_UNSUPPORTED, "no kernel fits T=%d H=%d K=%d R=%d in shared memory (kernel %d)", a->T, a->H,
               a->K, a->R, a->kernel);

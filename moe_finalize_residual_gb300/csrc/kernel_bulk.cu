@@ -156,7 +156,9 @@ __global__ void __launch_bounds__(32 * (2 + kBulkComputeWarps), 1) bulk_finalize
     }
   } else if (warp == 1) {
     // ---------------- copy warp ----------------
-    uint32_t pc = 0;  // stages issued so far
+    uint32_t pc = 0;        // stages issued so far
+    int ws = 0;             // the stage the next copies go to
+    uint32_t wround = 0;    // how many times the ring has been filled before (for the free-stage wait)
     bool ok = true;
     for (int i = 0; i < ntok && ok; ++i) {
       const int slot = i % kLists;
@@ -168,11 +170,14 @@ __global__ void __launch_bounds__(32 * (2 + kBulkComputeWarps), 1) bulk_finalize
         const int64_t off = static_cast<int64_t>(ps) * W * 2;
         const uint32_t bytes = static_cast<uint32_t>(min(W, H - ps * W)) * 2u;
         for (int j0 = 0; j0 < n; j0 += SR, ++pc) {
-          const int s = static_cast<int>(pc % static_cast<uint32_t>(NST));
-          const uint32_t use = pc / static_cast<uint32_t>(NST);
-          if (use > 0 && !warp_wait_phase(empty0 + 8u * s, (use & 1u) ^ 1u, abort_flag)) {
+          const int s = ws;
+          if (wround > 0 && !warp_wait_phase(empty0 + 8u * s, (wround & 1u) ^ 1u, abort_flag)) {
             ok = false;
             break;
+          }
+          if (++ws == NST) {
+            ws = 0;
+            ++wround;
           }
           const int cnt = min(SR, n - j0);
           const uint8_t* src = (lane < cnt) ? list[j0 + lane].src : nullptr;  // NULL: a closing entry, no data
@@ -221,7 +226,8 @@ __global__ void __launch_bounds__(32 * (2 + kBulkComputeWarps), 1) bulk_finalize
     float2 acc[Q * 4], S[Q * 4];
 #pragma unroll
     for (int i = 0; i < Q * 4; ++i) acc[i] = S[i] = make_float2(0.0f, 0.0f);
-    uint32_t cc = 0;  // stages consumed so far
+    int cs = 0;          // the stage the next rows are in
+    uint32_t cpar = 0;   // its barrier's phase parity
     bool ok = true;
     for (int i = 0; i < ntok && ok; ++i) {
       const int t = static_cast<int>(blockIdx.x) + i * G;
@@ -240,18 +246,20 @@ __global__ void __launch_bounds__(32 * (2 + kBulkComputeWarps), 1) bulk_finalize
 #pragma unroll
         for (int q = 0; q < Q; ++q)
           col_off[q] = ((cmask >> q) & 1u) ? static_cast<uint32_t>((jt + q * kNCT) * 16) : 0u;
-        for (int j0 = 0; j0 < n; j0 += SR, ++cc) {
-          const int s = static_cast<int>(cc % static_cast<uint32_t>(NST));
-          if (!warp_wait_phase(full0 + 8u * s, (cc / static_cast<uint32_t>(NST)) & 1u, abort_flag)) {
+        const uint32_t list_s = smem_addr(list);
+        for (int j0 = 0; j0 < n; j0 += SR) {
+          const int s = cs;
+          if (!warp_wait_phase(full0 + 8u * s, cpar, abort_flag)) {
             ok = false;
             break;
           }
           const int cnt = min(SR, n - j0);
-          for (int jj = 0; jj < cnt; ++jj) {
-            const uint4 ent = lds16(smem_addr(list + j0 + jj));  // source (unused here), scale, tag
+          uint32_t row = stage0 + static_cast<uint32_t>(s * SR * slot_bytes);  // the row's slot
+          uint32_t ent_s = list_s + 16u * j0;
+          for (int jj = 0; jj < cnt; ++jj, row += slot_bytes, ent_s += 16u) {
+            const uint4 ent = lds16(ent_s);  // source (unused here), scale, tag
             const float scale = __uint_as_float(ent.z);
             const uint32_t tag = ent.w;
-            const uint32_t row = stage0 + static_cast<uint32_t>((s * SR + jj) * slot_bytes);  // the row's slot
             if (!(tag & (kTagShared | kTagResidual))) {  // a routed row: acc += scale * row, fused
               const float2 sc = make_float2(scale, scale);
 #pragma unroll
@@ -310,6 +318,10 @@ __global__ void __launch_bounds__(32 * (2 + kBulkComputeWarps), 1) bulk_finalize
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(empty0 + 8u * s);
+          if (++cs == NST) {
+            cs = 0;
+            cpar ^= 1u;
+          }
         }
       }
       if (!ok) break;

@@ -303,9 +303,16 @@ template <typename A, int N>
 __device__ __forceinline__ void epilogue(const KParams& p, int64_t t, int h, bool active, const float x[N],
                                          const float g[N], float rstd, float qscale) {
   static_assert(N == 4 || N == 8, "4 or 8 elements per thread");
+  // (x * rstd) * gamma by packed FP32 multiplies (each lane rounded like __fmul_rn; two multiplies are
+  // never contracted).  Packing to act rounds each value to nearest-even, as rounding first would.
   float y[N];
+  const float2 r2 = make_float2(rstd, rstd);
 #pragma unroll
-  for (int i = 0; i < N; ++i) y[i] = Act<A>::round(__fmul_rn(__fmul_rn(x[i], rstd), g[i]));
+  for (int i = 0; i < N / 2; ++i) {
+    const float2 v = __fmul2_rn(__fmul2_rn(make_float2(x[2 * i], x[2 * i + 1]), r2), make_float2(g[2 * i], g[2 * i + 1]));
+    y[2 * i] = v.x;
+    y[2 * i + 1] = v.y;
+  }
   const int64_t e = t * p.H + h;
   if (active && p.norm_out != nullptr) {
     uint32_t w[N / 2];
@@ -316,6 +323,10 @@ __device__ __forceinline__ void epilogue(const KParams& p, int64_t t, int h, boo
     else
       *reinterpret_cast<uint2*>(p.norm_out + e * 2) = make_uint2(w[0], w[1]);
   }
+  if (p.quant == MFR_QUANT_NONE) return;
+  // The quantisers read the rounded norm_out values.
+#pragma unroll
+  for (int i = 0; i < N; ++i) y[i] = Act<A>::round(y[i]);
   if (p.quant == MFR_QUANT_FP8_E4M3) {
     if (active) {
 #pragma unroll

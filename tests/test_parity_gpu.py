@@ -373,13 +373,23 @@ def test_graph_replay_back_to_back(kernel):
 
 
 def test_kernel_choice_and_plan():
+    """The automatic choice follows the workload: the cluster kernel for small and medium batches and for
+    small rows, the bulk-copy kernel once every SM streams several whole tokens of large rows -- for the
+    decode rows (shared experts) and the bandwidth rows (none) alike."""
     import moe_finalize_residual_gb300 as mfr
-    small = on_gpu(synth.make_case("p", T=4, H=6144, K=8, R=4, E=64, shared=True))
-    big = synth.make_case("p", T=2048, H=6144, K=8, R=4, E=64, device="cuda")
-    p1 = mfr.moe_finalize_plan(partials_of(small), small.residual, small.gamma)
-    p2 = mfr.moe_finalize_plan(partials_of(big), big.residual, big.gamma)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def plan(T, H, shared, R=4, K=8):
+        c = synth.make_case("p", T=T, H=H, K=K, R=R, E=64, shared=shared, device="cuda")
+        return mfr.moe_finalize_plan(partials_of(c), c.residual, c.gamma)
+    p1 = plan(4, 6144, True)
     assert p1["kernel"] == "cluster" and p1["cluster"] >= 2 and p1["grid"] == 4 * p1["cluster"]
-    assert p2["kernel"] == "stream" and p2["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count * 2
+    for shared in (True, False):
+        for H in (6144, 7168):
+            assert plan(512, H, shared)["kernel"] == "cluster"
+            pb = plan(6 * sms + 8, H, shared)
+            assert pb["kernel"] == "bulk" and pb["grid"] == sms, pb
+    assert plan(6 * sms + 8, 2048, False)["kernel"] == "cluster"  # 4 KB rows: cluster kernel
 
 
 def test_gather_floor_copies_the_indexed_row():
