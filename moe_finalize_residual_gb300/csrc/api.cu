@@ -211,7 +211,16 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
   // token, each looping over several chunks.  More CTAs per token when shared memory is short.
   // Cluster sizes of 5-7 and 9-15 CTAs measured slower than the next smaller size in {1, 2, 3, 4, 8, 16}.
   const int c_raw = std::max(1, std::min(kMaxCluster, (MFR_CLUSTER_CTAS_PER_SM * d.sms) / std::max(1, a->T)));
-  const int c_goal = c_raw >= 16 ? 16 : c_raw >= 8 ? 8 : c_raw >= 4 ? 4 : c_raw;
+  int c_goal = c_raw >= 16 ? 16 : c_raw >= 8 ? 8 : c_raw >= 4 ? 4 : c_raw;
+  // One-chunk plans whose grid would put two CTAs on most SMs and one on the rest take half the cluster
+  // when that still covers the slice in one chunk with at most one CTA per SM: every SM then moves the
+  // same bytes (L2-warm: decode T=16 4.11 us with 8-CTA clusters against 4.22 with 16; top-22 H=2048
+  // T=16 5.12 against 5.34).  Not with fewer doubled SMs (decode T=12: 3.90 against 3.80), nor for top-k
+  // 9..16, whose wider block would take two rounds of loads (top-10 R=4 T=16: 5.25 against 4.73).
+  if (c_goal >= 4 && 2 * static_cast<int64_t>(a->T) * c_goal > 3 * static_cast<int64_t>(d.sms) &&
+      static_cast<int64_t>(a->T) * (c_goal / 2) <= d.sms && ceil_div(nvec, c_goal / 2) <= sv_max &&
+      (a->K <= 8 || a->K > 16))
+    c_goal /= 2;
   // Candidates in order of preference: c_goal, larger counts (when shared memory is short), then smaller
   // ones.  The first whose grid runs in one wave of resident clusters wins, else the one with the fewest
   // waves.  (The 16-routes-in-flight form takes about 120 registers a thread, so only one 448- or
@@ -238,7 +247,7 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
     // clusters (of C CTAs; single CTAs when C = 1) the GPU holds at once, for a form
     auto resident = [&](int f) {
-      const auto key = std::make_tuple(dev, a->act_dtype * 3 + f, C, block, smem);
+      const auto key = std::make_tuple(dev, a->act_dtype * 4 + f, C, block, smem);
       int n;
       {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -253,10 +262,17 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
       }
       return n;
     };
-    // One chunk: the wider register budget when it still runs in one wave, else the narrower one.
+    // One chunk: the wider register budget when it still runs in one wave, else the narrower one.  With
+    // at most 256 gathering threads on any SM, the latency form (route entries in registers, branch-free
+    // predicated loads): decode T=1 3.09 us against 3.41, T=8 3.50 against 3.72 (L2-warm); with more
+    // threads per SM it is slower (T=12, two CTAs on some SMs: 4.12 against 3.81; T=16, one 384-thread
+    // CTA per SM: 4.44 against 4.24).
     int form = kc == 16 ? kClusterForm16 : nch == 1 ? kClusterForm8OneChunk : kClusterForm8;
+    if (form == kClusterForm8OneChunk && a->K <= 8 &&
+        static_cast<int64_t>(block) * ceil_div(a->T * C, d.sms) <= 256)
+      form = kClusterForm8Latency;
     int n = resident(form);
-    if (form == kClusterForm8OneChunk && n < a->T) {
+    if ((form == kClusterForm8OneChunk || form == kClusterForm8Latency) && n < a->T) {
       form = kClusterForm8;
       n = resident(form);
     }

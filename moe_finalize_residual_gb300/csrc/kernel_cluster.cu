@@ -50,8 +50,33 @@ __device__ __forceinline__ void fill_routes(const KParams& p, const KPartial& P,
 }
 
 // Routes k0..k0+KC-1 of the table, all KC rows in flight together, then the FMA chain over them in
-// route order (rows of routes with index -1 are neither loaded nor added).  A route's table entry is
-// read again for its FMA, so the indices and scales need no registers while the loads are in flight.
+// route order (rows of routes with index -1 are neither loaded nor added).  The one-chunk form (small
+// batches, at most 256 gathering threads on an SM) keeps the KC table entries in registers and issues
+// the row loads under predicates, with no branch between them; the other forms read a route's entry
+// again for its FMA, so the indices and scales need no registers while the loads are in flight.
+template <typename A, int KC>
+__device__ __forceinline__ void gather_chain_regs(const KPartial& P, int H, int K, int vec, const int2* rt, int k0,
+                                                  float2 acc[4]) {
+  int2 e[KC];
+#pragma unroll
+  for (int j = 0; j < KC; ++j) e[j] = (k0 + j < K) ? rt[k0 + j] : make_int2(-1, 0);
+  const uint8_t* base = P.gemm2 + static_cast<int64_t>(vec) * 16;
+  const int64_t row_bytes = static_cast<int64_t>(H) * 2;
+  uint4 d[KC];
+#pragma unroll
+  for (int j = 0; j < KC; ++j) d[j] = ldg16_if(base + static_cast<int64_t>(max(e[j].x, 0)) * row_bytes, e[j].x >= 0);
+#pragma unroll
+  for (int j = 0; j < KC; ++j) {
+    if (e[j].x >= 0) {  // element pairs by the packed FMA, each lane rounded like fmaf
+      float2 x[4];
+      unpack_pairs<A>(d[j], x);
+      const float2 sc = make_float2(__int_as_float(e[j].y), __int_as_float(e[j].y));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = __ffma2_rn(sc, x[i], acc[i]);
+    }
+  }
+}
+
 template <typename A, int KC>
 __device__ __forceinline__ void gather_chain(const KPartial& P, int H, int K, int vec, const int2* rt, int k0,
                                              float2 acc[4]) {
@@ -102,7 +127,7 @@ __device__ __forceinline__ void cluster_exchange_wait(uint32_t bar) {
 #define MFR_CLUSTER_MIN_BLOCKS 2
 #endif
 
-template <typename A, int KC, int MINB>
+template <typename A, int KC, int MINB, bool REGS>
 __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -168,7 +193,10 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain<A, KC>(P, H, p.K, vec, rt, k0, acc);
+    if constexpr (REGS)
+      for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain_regs<A, KC>(P, H, p.K, vec, rt, k0, acc);
+    else
+      for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain<A, KC>(P, H, p.K, vec, rt, k0, acc);
     if (ch == 0) cp_async_wait_all();
     uint4* xr = &xch[(ch * p.R + r) * SV + v];
     float shv[8];
@@ -275,9 +303,9 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
   }
 }
 
-template <typename A, int KC, int MINB>
+template <typename A, int KC, int MINB, bool REGS = false>
 static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  auto kern = cluster_finalize_kernel<A, KC, MINB>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS>;
   static std::atomic<int> configured[64] = {};  // per device: the attributes are set (once is enough)
   int dev = 0;
   cudaGetDevice(&dev);
@@ -310,9 +338,9 @@ static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStr
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <typename A, int KC, int MINB>
+template <typename A, int KC, int MINB, bool REGS = false>
 static int max_active_clusters(const LaunchGeom& g) {
-  auto kern = cluster_finalize_kernel<A, KC, MINB>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaLaunchConfig_t cfg = {};
@@ -334,9 +362,9 @@ static int max_active_clusters(const LaunchGeom& g) {
   return n;
 }
 
-template <typename A, int KC, int MINB>
+template <typename A, int KC, int MINB, bool REGS = false>
 static int blocks_per_sm(const LaunchGeom& g) {
-  auto kern = cluster_finalize_kernel<A, KC, MINB>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, g.block, g.smem) != cudaSuccess) {
@@ -352,6 +380,7 @@ static cudaError_t launch_form(const KParams& p, const LaunchGeom& g, cudaStream
   switch (p.cluster_form) {
     case kClusterForm8: return launch_cluster<A, 8, MFR_CLUSTER_MIN_BLOCKS>(p, g, stream);
     case kClusterForm8OneChunk: return launch_cluster<A, 8, 1>(p, g, stream);
+    case kClusterForm8Latency: return launch_cluster<A, 8, 1, true>(p, g, stream);
     default: return launch_cluster<A, 16, 1>(p, g, stream);
   }
 }
@@ -365,6 +394,7 @@ static int blocks_per_sm_form(int form, const LaunchGeom& g) {
   switch (form) {
     case kClusterForm8: return blocks_per_sm<A, 8, MFR_CLUSTER_MIN_BLOCKS>(g);
     case kClusterForm8OneChunk: return blocks_per_sm<A, 8, 1>(g);
+    case kClusterForm8Latency: return blocks_per_sm<A, 8, 1, true>(g);
     default: return blocks_per_sm<A, 16, 1>(g);
   }
 }
@@ -378,6 +408,7 @@ static int max_active_clusters_form(int form, const LaunchGeom& g) {
   switch (form) {
     case kClusterForm8: return max_active_clusters<A, 8, MFR_CLUSTER_MIN_BLOCKS>(g);
     case kClusterForm8OneChunk: return max_active_clusters<A, 8, 1>(g);
+    case kClusterForm8Latency: return max_active_clusters<A, 8, 1, true>(g);
     default: return max_active_clusters<A, 16, 1>(g);
   }
 }

@@ -271,6 +271,18 @@ __device__ __forceinline__ void unpack8(uint4 raw, float v[8]) {
 }
 
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+// 16-byte read-only global load under a predicate, with no branch (zeros when `on` is false; the address
+// is then not read).  Volatile, so it stays after the dependency wait, but with no memory clobber, so the
+// loads of a round issue back to back.
+__device__ __forceinline__ uint4 ldg16_if(const uint8_t* p, bool on) {
+  uint4 v;
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n mov.b32 %0, 0;\n mov.b32 %1, 0;\n mov.b32 %2, 0;\n"
+      " mov.b32 %3, 0;\n @q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n}\n"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "r"(static_cast<int>(on)));
+  return v;
+}
 
 __device__ __forceinline__ float load_scale(const void* base, int64_t i, int dtype) {
   if (base == nullptr) return 1.0f;  // absent expert scales read as 1.0

@@ -50,7 +50,9 @@ cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchG
 // Cluster kernel forms: 8 routes in flight per thread with the register budget of two 512-thread CTAs
 // per SM (plans that loop over chunks); 8 in flight with a wider register budget (one-chunk plans, whose
 // CTAs are small); 16 in flight.
-enum ClusterForm { kClusterForm8 = 0, kClusterForm8OneChunk = 1, kClusterForm16 = 2 };
+// The latency form is the one-chunk form with the route entries held in registers and branch-free
+// predicated row loads, for grids that put at most 256 gathering threads on an SM.
+enum ClusterForm { kClusterForm8 = 0, kClusterForm8OneChunk = 1, kClusterForm16 = 2, kClusterForm8Latency = 3 };
 int cluster_kernel_max_active_clusters(int act_dtype, int form, const LaunchGeom& g);
 int cluster_kernel_blocks_per_sm(int act_dtype, int form, const LaunchGeom& g);
 cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);

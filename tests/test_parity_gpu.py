@@ -553,6 +553,32 @@ def test_residual_out_in_place(T, kernel):
     assert ulp_distance(bits16(norm), want["norm_out"]).max() <= 1
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("R", [2, 4])
+def test_tp_one_shot_emulated_on_one_gpu(R, kernel):
+    """The tensor-parallel path (moe_finalize_residual_gb300.tp) with its R ranks emulated in turn on the
+    one GPU: rank r's finalize-only call gives its rounded partial p_r, the exchange hands every rank the
+    slots p_0..p_{R-1} (gathered here without a collective), and every rank's fused call over the
+    exchanged slots gives the oracle's R-partial residual_out bit for bit and its norm_out within 1 ulp."""
+    import moe_finalize_residual_gb300 as mfr
+    from moe_finalize_residual_gb300 import tp
+    case = synth.make_case("tp", T=37, H=2048, K=8, R=R, E=64, rsf=2.5, shared=True, mask_quarter=True,
+                           scale_dtype=torch.float32)
+    g = on_gpu(case)
+    parts = partials_of(g)
+    slots = [mfr.moe_finalize_routed([parts[r]], routed_scaling_factor=g.rsf, kernel=kernel) for r in range(R)]
+    want = oracle.finalize(case)
+    for r in range(R):
+        def exchange(p_r, group, r=r):
+            assert torch.equal(p_r, slots[r])  # this rank's own row, finalized again by the protocol
+            return slots
+        ro, no, _, _ = tp.tp_finalize_fused(parts[r], g.residual, g.gamma, routed_scaling_factor=g.rsf, eps=g.eps,
+                                            exchange=exchange, kernel=kernel)
+        torch.cuda.synchronize()
+        from helpers import Result
+        check_against_oracle(case, Result(bits16(ro), bits16(no), None, None, True), want)
+
+
 # ------------------------------------------------------------------------------------------------------
 # Finalize-only mode: the rounded rank sum S (p_0 for one partial), no residual / RMSNorm / quant.
 
