@@ -144,8 +144,9 @@ typedef struct {
   int32_t quant_mode;        /* mfr_quant                                                           */
   int32_t sf_layout;         /* mfr_sf_layout (NVFP4 only)                                          */
   const float* quant_scale;  /* device fp32 scalar: FP8 encode scale s, or NVFP4 global scale g     */
-  void* quant_out;           /* device: FP8 [T, H] bytes; NVFP4 [T, H/2] bytes, even element in the
-                                low nibble.  Required iff quant_mode != NONE                        */
+  void* quant_out;           /* device: FP8 [T, H] bytes (8-byte aligned); NVFP4 [T, H/2] bytes, even
+                                element in the low nibble (4-byte aligned).  Required iff
+                                quant_mode != NONE                                                  */
   void* sf_out;              /* device NVFP4 block scales (e4m3 bytes), moe_finalize_sf_bytes()
                                 bytes; padding bytes are not written.  Required iff NVFP4           */
   uint32_t flags;            /* MFR_FLAG_*                                                          */

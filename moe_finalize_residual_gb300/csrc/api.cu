@@ -118,8 +118,9 @@ int validate(const mfr_args* a) {
       return fail(MFR_ERR_INVALID_ARG, "quantisation needs quant_out and quant_scale");
     if (a->quant_mode == MFR_QUANT_NVFP4 && a->sf_out == nullptr)
       return fail(MFR_ERR_INVALID_ARG, "NVFP4 needs sf_out (moe_finalize_sf_bytes bytes)");
-    if (!aligned(a->quant_scale, 4) || !aligned(a->quant_out, a->quant_mode == MFR_QUANT_FP8_E4M3 ? 4 : 2))
-      return fail(MFR_ERR_INVALID_ARG, "quant_scale or quant_out misaligned");
+    // the epilogue writes 8 FP8 bytes or 4 NVFP4 bytes per thread in one store
+    if (!aligned(a->quant_scale, 4) || !aligned(a->quant_out, a->quant_mode == MFR_QUANT_FP8_E4M3 ? 8 : 4))
+      return fail(MFR_ERR_INVALID_ARG, "quant_scale (4 bytes) or quant_out (8 bytes FP8, 4 bytes NVFP4) misaligned");
   }
   if (a->residual_out == nullptr && a->norm_out == nullptr && a->quant_mode == MFR_QUANT_NONE &&
       a->finalize_out == nullptr)
@@ -379,14 +380,32 @@ bool plan_stream(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, La
   return false;
 }
 
-// Bulk-copy kernel: persistent CTAs (one per SM) of a routing warp, a copy warp and kBulkComputeWarps
-// compute warps,
+// Bulk-copy kernel: persistent CTAs (one per SM) of a routing warp, a copy warp and 8 to 14 compute
+// warps (as many as fill their columns most evenly: the row's 16-byte columns over the threads, whole
+// columns per thread; ties to more warps), 
 // each CTA finalizing whole tokens in turn.  A pass covers the whole row when the compute threads can
 // hold it in kBulkMaxColumns 16-byte columns each, else the row is cut into equal passes (multiples of
 // 16 elements).  The ring takes stages of SR row slots: four stages, each with as many rows as shared
 // memory allows (at least one, at most 8), fewer stages only when even one row per stage does not fit.
 bool plan_bulk(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
-  const int nct = 32 * kBulkComputeWarps;
+  // Compute warps: decode H=6144 (768 columns) 12 warps, two columns each, 80.3 us at T=1024 against
+  // 81.8 with 14; H=7168 (896 columns) 14 warps, 84.6 us against 86.7 with 12 (L2-cold).
+  int ncw = kBulkMaxComputeWarps;
+  {
+    double best = -1.0;
+    for (int w = 8; w <= kBulkMaxComputeWarps; w += 2) {
+      const int nt = 32 * w;
+      const int np = ceil_div(a->H, 8 * nt * kBulkMaxColumns);
+      const int wp = np == 1 ? a->H : align_up(ceil_div(a->H, np), 16);
+      const int q = ceil_div(ceil_div(wp, 8), nt);
+      const double use = static_cast<double>(ceil_div(wp, 8)) / (static_cast<double>(q) * nt);
+      if (use >= best) {
+        best = use;
+        ncw = w;
+      }
+    }
+  }
+  const int nct = 32 * ncw;
   const int block = 64 + nct;  // a routing warp, a copy warp and the compute warps
   const int max_pass = 8 * nct * kBulkMaxColumns;
   const int npass = ceil_div(a->H, max_pass);
@@ -425,6 +444,7 @@ bool plan_bulk(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, Laun
     p->stage_rows = sr;
     p->stage_bytes = slot_bytes;
     p->cols_per_thread = Q;
+    p->compute_warps = ncw;
     p->ring_bytes = ring_bytes;
     p->off_bar = off_bar;
     p->off_stage = off_stage;

@@ -40,8 +40,6 @@ namespace {
 
 constexpr uint64_t kLimitNs = 2000000000ull;
 constexpr uint32_t kSleepHintNs = 20000;  // a waiting thread sleeps until the phase completes, or about 20 us
-constexpr int kNCW = kBulkComputeWarps;  // compute warps
-constexpr int kNCT = 32 * kNCW;          // compute threads
 constexpr int kLists = 4;                // row lists (tokens) in the ring
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or the limit ran out (then it
@@ -88,15 +86,18 @@ __device__ __forceinline__ void flush(float2 acc[Q * 4], float2 S[Q * 4], bool s
 
 }  // namespace
 
-// Q: 16-byte columns per compute thread per pass (the pass covers 8 * kNCT * Q elements at most).
+// Q: 16-byte columns per compute thread per pass (the pass covers 8 * NCT * Q elements at most, NCT the
+// compute threads of the launch: p.compute_warps warps, chosen so the columns fill them evenly).
 template <typename A, int Q>
-__global__ void __launch_bounds__(32 * (2 + kBulkComputeWarps), 1) bulk_finalize_kernel(const __grid_constant__ KParams p) {
+__global__ void __launch_bounds__(32 * (2 + kBulkMaxComputeWarps), 1) bulk_finalize_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int H = p.H, W = p.chunk;
   const int npass = (H + W - 1) / W;
   const int NST = p.stages, SR = p.stage_rows;
+  const int kNCW = p.compute_warps;  // compute warps
+  const int kNCT = 32 * kNCW;        // compute threads
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
   const uint32_t full0 = smem_addr(bars);                 // NST: a stage's rows have landed
@@ -112,15 +113,15 @@ __global__ void __launch_bounds__(32 * (2 + kBulkComputeWarps), 1) bulk_finalize
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, kNCW);
+      mbar_init(empty0 + 8u * s, static_cast<uint32_t>(kNCW));
     }
     for (int i = 0; i < kLists; ++i) {
       mbar_init(lfull0 + 8u * i, 1);
-      mbar_init(lempty0 + 8u * i, kNCW + 1);  // the compute warps and the copy warp read a list
+      mbar_init(lempty0 + 8u * i, static_cast<uint32_t>(kNCW) + 1u);  // the compute warps and the copy warp
     }
     // (the failure-detection test hook adds an arrival that never comes, so every wait on these runs out)
-    mbar_init(meet0, kNCW + p.test_token_bar_extra);
-    mbar_init(meet0 + 8u, kNCW + p.test_token_bar_extra);
+    mbar_init(meet0, static_cast<uint32_t>(kNCW) + p.test_token_bar_extra);
+    mbar_init(meet0 + 8u, static_cast<uint32_t>(kNCW) + p.test_token_bar_extra);
     *abort_flag = 0;
     fence_mbar_init();
   }

@@ -76,6 +76,7 @@ struct KParams {
   // bulk-copy kernel (also chunk = pass width, stages, stage_bytes = one row slot, ring_bytes, offsets)
   int32_t stage_rows;       // rows per stage (one mbarrier per stage)
   int32_t cols_per_thread;  // 16-byte columns per compute thread per pass (template parameter)
+  int32_t compute_warps;    // bulk-copy kernel: compute warps of the launch
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -341,16 +342,20 @@ __device__ __forceinline__ void epilogue(const KParams& p, int64_t t, int h, boo
   for (int i = 0; i < N; ++i) y[i] = Act<A>::round(y[i]);
   if (p.quant == MFR_QUANT_FP8_E4M3) {
     if (active) {
+      uint32_t q[N / 4];
 #pragma unroll
       for (int j = 0; j < N / 4; ++j) {
-        uint32_t q = 0;
+        q[j] = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          q |= static_cast<uint32_t>(
-                   __nv_cvt_float_to_fp8(__fmul_rn(y[4 * j + i], qscale), __NV_SATFINITE, __NV_E4M3))
-               << (8 * i);
-        *reinterpret_cast<uint32_t*>(p.quant_out + e + 4 * j) = q;
+          q[j] |= static_cast<uint32_t>(
+                      __nv_cvt_float_to_fp8(__fmul_rn(y[4 * j + i], qscale), __NV_SATFINITE, __NV_E4M3))
+                  << (8 * i);
       }
+      if constexpr (N == 8)  // one 8-byte store (e is a multiple of 8)
+        *reinterpret_cast<uint2*>(p.quant_out + e) = make_uint2(q[0], q[1]);
+      else
+        *reinterpret_cast<uint32_t*>(p.quant_out + e) = q[0];
     }
   } else if (p.quant == MFR_QUANT_NVFP4) {
     float amax = 0.0f;
@@ -365,14 +370,16 @@ __device__ __forceinline__ void epilogue(const KParams& p, int64_t t, int h, boo
     const float sf_val = __half2float(__half(__nv_cvt_fp8_to_halfraw(sf, __NV_E4M3)));
     const float es = (sf_val == 0.0f) ? 0.0f : __fdiv_rn(qscale, sf_val);
     if (active) {
+      uint32_t codes = 0;  // N / 2 bytes, even element in the low nibble
 #pragma unroll
-      for (int j = 0; j < N / 4; ++j) {
-        const uint32_t c01 = __nv_cvt_float2_to_fp4x2(
-            make_float2(__fmul_rn(y[4 * j], es), __fmul_rn(y[4 * j + 1], es)), __NV_E2M1, cudaRoundNearest);
-        const uint32_t c23 = __nv_cvt_float2_to_fp4x2(
-            make_float2(__fmul_rn(y[4 * j + 2], es), __fmul_rn(y[4 * j + 3], es)), __NV_E2M1, cudaRoundNearest);
-        *reinterpret_cast<uint16_t*>(p.quant_out + e / 2 + 2 * j) = static_cast<uint16_t>(c01 | (c23 << 8));
-      }
+      for (int j = 0; j < N / 2; ++j)
+        codes |= static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(
+                     make_float2(__fmul_rn(y[2 * j], es), __fmul_rn(y[2 * j + 1], es)), __NV_E2M1, cudaRoundNearest))
+                 << (8 * j);
+      if constexpr (N == 8)  // one 4-byte store (e / 2 is a multiple of 4)
+        *reinterpret_cast<uint32_t*>(p.quant_out + e / 2) = codes;
+      else
+        *reinterpret_cast<uint16_t*>(p.quant_out + e / 2) = static_cast<uint16_t>(codes);
       if ((h & 15) == 0) p.sf_out[sf_offset(t, h >> 4, p.H, p.sf_layout)] = sf;
     }
   }

@@ -30,11 +30,9 @@ constexpr int kStreamColumns = MFR_STREAM_COLUMNS;  // 16-byte columns per compu
 static_assert(kStreamLists % kStreamGroups == 0, "a list slot must return to the group that used it");
 static_assert(kStreamGroups == 1 || kStreamGroups == 2, "the stream kernel is built for one or two groups");
 constexpr int kClusterMaxThreads = 512;             // R groups of SV threads
-// Bulk-copy streaming kernel: a routing warp, a copy warp and this many compute warps.
-#ifndef MFR_BULK_COMPUTE_WARPS
-#define MFR_BULK_COMPUTE_WARPS 14
-#endif
-constexpr int kBulkComputeWarps = MFR_BULK_COMPUTE_WARPS;
+// Bulk-copy streaming kernel: a routing warp, a copy warp and 8 to kBulkMaxComputeWarps compute warps
+// (the planner's choice per row width).
+constexpr int kBulkMaxComputeWarps = 14;
 constexpr int kBulkMaxColumns = 4;                  // 16-byte columns per compute thread per pass
 
 

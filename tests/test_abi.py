@@ -113,6 +113,8 @@ BAD = [
     dict(quant_mode=1), dict(quant_mode=2, quant_scale=0xF00000, quant_out=0xF10000),
     dict(quant_mode=2, quant_scale=0xF00000, quant_out=0xF10000, sf_out=0xF20000, sf_layout=2),
     dict(quant_mode=2, quant_scale=0xF00000, quant_out=0xF10000, sf_out=0xF20000, H=264),
+    dict(quant_mode=1, quant_scale=0xF00000, quant_out=0xF10004),  # FP8 output needs 8-byte alignment
+    dict(quant_mode=2, quant_scale=0xF00000, quant_out=0xF10002, sf_out=0xF20000),  # NVFP4: 4-byte alignment
     dict(partials=None),
 ]
 
