@@ -200,13 +200,15 @@ constexpr int kMaxCluster = MFR_CLUSTER_MAX_SIZE;
 // R*SV <= kClusterMaxThreads.
 // This plans one form of the kernel (kc routes in flight per thread) and reports how many waves of
 // resident clusters its grid takes.
-bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, KParams* p, LaunchGeom* g,
+bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, int split, KParams* p, LaunchGeom* g,
                        int64_t* waves_out) {
   const int nvec = a->H / 8;
   const int unit = (a->H % 16 == 0) ? 2 : 1;  // slices start on 16-element blocks when H allows
   const int R = a->R;
-  const int sv_max = (kClusterMaxThreads / R) / unit * unit;
-  const int sv_soft = std::min(sv_max, std::max(unit, (MFR_CLUSTER_BLOCK / R) / unit * unit));
+  const int RS = R * split;                   // thread groups: partials x route groups (split form)
+  const int sv_max = (kClusterMaxThreads / RS) / unit * unit;
+  if (sv_max < unit) return false;
+  const int sv_soft = std::min(sv_max, std::max(unit, (MFR_CLUSTER_BLOCK / RS) / unit * unit));
   // About two CTAs per SM in all: c_goal CTAs per token, each covering nchunk chunks of sv vectors.
   // Few tokens: one chunk, the row spread over up to kMaxCluster CTAs.  More tokens: fewer CTAs per
   // token, each looping over several chunks.  More CTAs per token when shared memory is short.
@@ -239,11 +241,13 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     const int nch = ceil_div(nvec, cg * sv);
     const int C = ceil_div(nvec, nch * sv);
     if (C > kMaxCluster || static_cast<int64_t>(a->T) * C > INT32_MAX) continue;  // grid.x is an int
+    if (split > 1 && nch != 1) continue;  // the split form covers its slice in one chunk
     const int sv_fit = align_up(ceil_div(nvec, C * nch), unit);  // even slices
-    const int block = align_up(sv_fit * R, 32);
+    const int block = align_up(sv_fit * RS, 32);
     const int off_red = align_up((R + 2) * nch * sv_fit * 16, 16);
     const int off_routes = align_up(off_red + 56 * 4, 16);  // 50 floats, then the exchange mbarrier
-    const int smem = align_up(off_routes + R * a->K * 8, 16);
+    const int off_split = align_up(off_routes + R * a->K * 8, 16);
+    const int smem = align_up(off_split + (split > 1 ? R * (split - 1) * 8 * sv_fit * 16 : 0), 16);
     if (smem > d.smem_optin) continue;
     LaunchGeom geo{a->T * C, block, C, smem, d.smem_optin};
     // clusters (of C CTAs; single CTAs when C = 1) the GPU holds at once, for a form
@@ -268,7 +272,7 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     // predicated loads): decode T=1 3.09 us against 3.41, T=8 3.50 against 3.72 (L2-warm); with more
     // threads per SM it is slower (T=12, two CTAs on some SMs: 4.12 against 3.81; T=16, one 384-thread
     // CTA per SM: 4.44 against 4.24).
-    int form = kc == 16 ? kClusterForm16 : nch == 1 ? kClusterForm8OneChunk : kClusterForm8;
+    int form = split > 1 ? kClusterForm8Split : kc == 16 ? kClusterForm16 : nch == 1 ? kClusterForm8OneChunk : kClusterForm8;
     if (form == kClusterForm8OneChunk && a->K <= 8 &&
         static_cast<int64_t>(block) * ceil_div(a->T * C, d.sms) <= 256)
       form = kClusterForm8Latency;
@@ -290,6 +294,8 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
     // 4 bytes from every CTA of the cluster (and 4 that never come under the timeout test hook)
     p->xch_tx_bytes = 4u * C + ((a->flags & MFR_FLAG_TEST_EXCHANGE_TIMEOUT) ? 4u : 0u);
     p->off_routes = off_routes;
+    p->route_groups = split;
+    p->off_split = off_split;
     *g = geo;
     *waves_out = waves;
     if (waves == 1) break;
@@ -305,12 +311,21 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
 // T=128: 5.4 against 7.3).  Larger top-k: sixteen in flight.
 bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
   int64_t waves = 0;
-  if (a->K <= 8) return plan_cluster_form(a, d, dev, 8, p, g, &waves);
-  const bool ok16 = plan_cluster_form(a, d, dev, 16, p, g, &waves);
+  if (a->K <= 8) return plan_cluster_form(a, d, dev, 8, 1, p, g, &waves);
+  if (a->K > 16) {  // the routes of a partial split over thread groups, when that plans one chunk in one wave
+    KParams ps = *p;
+    LaunchGeom gs{};
+    if (plan_cluster_form(a, d, dev, 8, ceil_div(a->K, 8), &ps, &gs, &waves) && waves == 1) {
+      *p = ps;
+      *g = gs;
+      return true;
+    }
+  }
+  const bool ok16 = plan_cluster_form(a, d, dev, 16, 1, p, g, &waves);
   if (a->K > 16 || (ok16 && g->block < 384 && waves == 1)) return ok16;
   KParams p8 = *p;
   LaunchGeom g8{};
-  if (plan_cluster_form(a, d, dev, 8, &p8, &g8, &waves)) {
+  if (plan_cluster_form(a, d, dev, 8, 1, &p8, &g8, &waves)) {
     *p = p8;
     *g = g8;
     return true;

@@ -127,7 +127,10 @@ __device__ __forceinline__ void cluster_exchange_wait(uint32_t bar) {
 #define MFR_CLUSTER_MIN_BLOCKS 2
 #endif
 
-template <typename A, int KC, int MINB, bool REGS>
+// SPLIT (one chunk, top-k > 16): each partial's routes are split over S = p.route_groups thread groups of
+// SV threads, group s loading routes 8s .. 8s+7 of its vector, so every row is in flight in one round;
+// groups s > 0 stage their raw rows in shared memory and group 0 runs the whole chain in route order.
+template <typename A, int KC, int MINB, bool REGS, bool SPLIT = false>
 __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -139,19 +142,23 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
   const int t = static_cast<int>(blockIdx.x / C);
   const int H = p.H;
   const int nvec = H >> 3;
-  const int r = tid / SV;                       // partial of this thread's group
-  const int v = tid - r * SV;
+  const int S = SPLIT ? p.route_groups : 1;     // route groups per partial
+  const int grp = tid / SV;                     // (partial, route group) of this thread
+  const int r = SPLIT ? grp / S : grp;          // partial of this thread's group
+  const int sg = SPLIT ? grp - r * S : 0;       // its route group: routes 8 * sg .. 8 * sg + 7
+  const int v = tid - grp * SV;
   const int vec0 = static_cast<int>(crank) * NCH * SV + v;  // chunk ch holds vector vec0 + ch * SV
-  const bool in_group = r < p.R;
+  const bool in_part = r < p.R;                 // loads rows of partial r
+  const bool in_group = in_part && sg == 0;     // finishes partial r's vector v
   uint4* xch = reinterpret_cast<uint4*>(smem);                // [NCH][R][SV] shared rows, then partial rows
   uint4* res_s = xch + NCH * p.R * SV;                        // [NCH][SV] residual slices, then residual_out
   uint4* gam_s = res_s + NCH * SV;                            // [NCH][SV] gamma slices
   float* red = reinterpret_cast<float*>(smem + p.off_red);    // [0,32) warp sums, [32,34) unused,
                                                               // [34,50) the cluster's CTA sums by rank,
                                                               // [52,54) the exchange's mbarrier
-  const KPartial& P = p.part[in_group ? r : 0];
+  const KPartial& P = p.part[in_part ? r : 0];
   const bool has_shared = in_group && ((p.shared_mask >> r) & 1u);
-  const bool lead_group = r == 0;               // group 0 finishes the token
+  const bool lead_group = r == 0 && sg == 0;    // partial 0's group 0 copies the residual and gamma
 
   // Every CTA of the cluster arrives here on entry; the matching wait comes before the first write into
   // a peer's shared memory, so no CTA writes into one that has not started.
@@ -164,10 +171,10 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
     mbar_arrive_expect_tx(xbar, p.xch_tx_bytes);
   }
   if (C > 1 && !p.fin_only) cluster_arrive_relaxed();
-  int2* rt = reinterpret_cast<int2*>(smem + p.off_routes) + (in_group ? r : 0) * p.K;  // this partial's routes
-  if (p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
+  int2* rt = reinterpret_cast<int2*>(smem + p.off_routes) + (in_part ? r : 0) * p.K;  // this partial's routes
+  if (p.routing_early && in_part) fill_routes(p, P, t, sg * SV + v, S * SV, rt);
   if (p.pdl) pdl_wait();
-  if (!p.routing_early && in_group) fill_routes(p, P, t, v, SV, rt);
+  if (!p.routing_early && in_part) fill_routes(p, P, t, sg * SV + v, S * SV, rt);
 
   // Rows that do not depend on the routing go out first, every chunk's, straight into shared memory.
   // A thread reads a shared row only after waiting for its own copies; the residual and gamma slices
@@ -187,6 +194,68 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
 
   // Each chunk: the partial's FMA chain over its routes, times the routed scaling factor, plus the
   // shared row, rounded once (the partial row p_r), into the chunk's exchange buffer.
+  if constexpr (SPLIT) {
+    // One chunk.  Every group loads its 8 routes at once; groups s > 0 stage the raw rows, group 0 adds its
+    // own, then (after the barrier) the staged ones, in route order.
+    uint4* stage = reinterpret_cast<uint4*>(smem + p.off_split);  // [R][S-1][8][SV]
+    const bool live = in_part && vec0 < nvec;
+    uint4 d[8];
+    const uint8_t* base = P.gemm2 + static_cast<int64_t>(vec0) * 16;
+    const int64_t row_bytes = static_cast<int64_t>(H) * 2;
+    int2 e[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = 8 * sg + j;
+      e[j] = (live && k < p.K) ? rt[k] : make_int2(-1, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d[j] = ldg16_if(base + static_cast<int64_t>(max(e[j].x, 0)) * row_bytes, e[j].x >= 0);
+    if (sg > 0 && live) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (e[j].x >= 0) stage[((r * (S - 1) + sg - 1) * 8 + j) * SV + v] = d[j];
+    }
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+    if (in_group && live) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (e[j].x >= 0) {
+          float2 x[4];
+          unpack_pairs<A>(d[j], x);
+          const float2 sc = make_float2(__int_as_float(e[j].y), __int_as_float(e[j].y));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = __ffma2_rn(sc, x[i], acc[i]);
+        }
+      }
+    }
+    __syncthreads();  // the staged rows are written
+    if (in_group && live) {
+      for (int k = 8; k < p.K; ++k) {
+        const int2 ek = rt[k];
+        if (ek.x >= 0) {
+          float2 x[4];
+          unpack_pairs<A>(stage[((r * (S - 1) + k / 8 - 1) * 8 + (k & 7)) * SV + v], x);
+          const float2 sc = make_float2(__int_as_float(ek.y), __int_as_float(ek.y));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = __ffma2_rn(sc, x[i], acc[i]);
+        }
+      }
+      cp_async_wait_all();
+      uint4* xr = &xch[r * SV + v];
+      float shv[8];
+      unpack8<A>(*xr, shv);
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a[i] = __fmul_rn((i & 1) ? acc[i >> 1].y : acc[i >> 1].x, p.rsf);
+        if (has_shared) a[i] = __fadd_rn(a[i], shv[i]);
+      }
+      *xr = make_uint4(Act<A>::pack(a[0], a[1]), Act<A>::pack(a[2], a[3]), Act<A>::pack(a[4], a[5]),
+                       Act<A>::pack(a[6], a[7]));
+    }
+  } else
   for (int ch = 0; ch < NCH; ++ch) {
     const int vec = vec0 + ch * SV;
     if (!in_group || vec >= nvec) break;
@@ -303,9 +372,9 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
   }
 }
 
-template <typename A, int KC, int MINB, bool REGS = false>
+template <typename A, int KC, int MINB, bool REGS = false, bool SPLIT = false>
 static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStream_t stream) {
-  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS, SPLIT>;
   static std::atomic<int> configured[64] = {};  // per device: the attributes are set (once is enough)
   int dev = 0;
   cudaGetDevice(&dev);
@@ -338,9 +407,9 @@ static cudaError_t launch_cluster(const KParams& p, const LaunchGeom& g, cudaStr
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <typename A, int KC, int MINB, bool REGS = false>
+template <typename A, int KC, int MINB, bool REGS = false, bool SPLIT = false>
 static int max_active_clusters(const LaunchGeom& g) {
-  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS, SPLIT>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaLaunchConfig_t cfg = {};
@@ -362,9 +431,9 @@ static int max_active_clusters(const LaunchGeom& g) {
   return n;
 }
 
-template <typename A, int KC, int MINB, bool REGS = false>
+template <typename A, int KC, int MINB, bool REGS = false, bool SPLIT = false>
 static int blocks_per_sm(const LaunchGeom& g) {
-  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS>;
+  auto kern = cluster_finalize_kernel<A, KC, MINB, REGS, SPLIT>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_optin);
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, g.block, g.smem) != cudaSuccess) {
@@ -381,6 +450,7 @@ static cudaError_t launch_form(const KParams& p, const LaunchGeom& g, cudaStream
     case kClusterForm8: return launch_cluster<A, 8, MFR_CLUSTER_MIN_BLOCKS>(p, g, stream);
     case kClusterForm8OneChunk: return launch_cluster<A, 8, 1>(p, g, stream);
     case kClusterForm8Latency: return launch_cluster<A, 8, 1, true>(p, g, stream);
+    case kClusterForm8Split: return launch_cluster<A, 8, 1, false, true>(p, g, stream);
     default: return launch_cluster<A, 16, 1>(p, g, stream);
   }
 }
@@ -395,6 +465,7 @@ static int blocks_per_sm_form(int form, const LaunchGeom& g) {
     case kClusterForm8: return blocks_per_sm<A, 8, MFR_CLUSTER_MIN_BLOCKS>(g);
     case kClusterForm8OneChunk: return blocks_per_sm<A, 8, 1>(g);
     case kClusterForm8Latency: return blocks_per_sm<A, 8, 1, true>(g);
+    case kClusterForm8Split: return blocks_per_sm<A, 8, 1, false, true>(g);
     default: return blocks_per_sm<A, 16, 1>(g);
   }
 }
@@ -409,6 +480,7 @@ static int max_active_clusters_form(int form, const LaunchGeom& g) {
     case kClusterForm8: return max_active_clusters<A, 8, MFR_CLUSTER_MIN_BLOCKS>(g);
     case kClusterForm8OneChunk: return max_active_clusters<A, 8, 1>(g);
     case kClusterForm8Latency: return max_active_clusters<A, 8, 1, true>(g);
+    case kClusterForm8Split: return max_active_clusters<A, 8, 1, false, true>(g);
     default: return max_active_clusters<A, 16, 1>(g);
   }
 }

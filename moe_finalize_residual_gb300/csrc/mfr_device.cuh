@@ -61,6 +61,8 @@ struct KParams {
   int32_t route_batch;    // cluster kernel: routes in flight per thread (8 or 16; larger top-k in rounds)
   int32_t cluster_form;   // cluster kernel: the compiled form to launch (ClusterForm)
   int32_t off_routes;     // cluster kernel: shared-memory route table [R][K] (row index or -1, scale)
+  int32_t route_groups;   // cluster kernel, split form: thread groups per partial (8 routes each)
+  int32_t off_split;      // cluster kernel, split form: staged rows [R][route_groups-1][8][slice_vec]
   int32_t off_red;
   uint32_t xch_tx_bytes;  // cluster kernel: bytes the exchange barrier expects (4 per CTA of the cluster)
   // stream kernel

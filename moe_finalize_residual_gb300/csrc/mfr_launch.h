@@ -50,7 +50,14 @@ cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchG
 // CTAs are small); 16 in flight.
 // The latency form is the one-chunk form with the route entries held in registers and branch-free
 // predicated row loads, for grids that put at most 256 gathering threads on an SM.
-enum ClusterForm { kClusterForm8 = 0, kClusterForm8OneChunk = 1, kClusterForm16 = 2, kClusterForm8Latency = 3 };
+// The split form (one chunk, top-k > 16) spreads each partial's routes over several thread groups.
+enum ClusterForm {
+  kClusterForm8 = 0,
+  kClusterForm8OneChunk = 1,
+  kClusterForm16 = 2,
+  kClusterForm8Latency = 3,
+  kClusterForm8Split = 4
+};
 int cluster_kernel_max_active_clusters(int act_dtype, int form, const LaunchGeom& g);
 int cluster_kernel_blocks_per_sm(int act_dtype, int form, const LaunchGeom& g);
 cudaError_t launch_stream_kernel(int act_dtype, const KParams& p, const LaunchGeom& g, cudaStream_t stream);
