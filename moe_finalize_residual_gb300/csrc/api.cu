@@ -312,7 +312,10 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
 bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
   int64_t waves = 0;
   if (a->K <= 8) return plan_cluster_form(a, d, dev, 8, 1, p, g, &waves);
-  if (a->K > 16) {  // the routes of a partial split over thread groups, when that plans one chunk in one wave
+  // Top-k > 8: the routes of a partial split over thread groups, when that plans one chunk in one wave.
+  // L2-warm, same box: top-32 H=4096 T=1 5.77 -> 4.35 us; top-22 H=2048 T=1 5.11 -> 3.71; top-16 H=3584
+  // T=1 4.10 -> 3.40, T=64 4.52 -> 4.12; top-10 R=2 T=1 3.63 -> 3.30 (never slower where it applies).
+  if (a->K > 8) {
     KParams ps = *p;
     LaunchGeom gs{};
     if (plan_cluster_form(a, d, dev, 8, ceil_div(a->K, 8), &ps, &gs, &waves) && waves == 1) {

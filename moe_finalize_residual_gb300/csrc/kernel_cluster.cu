@@ -127,7 +127,7 @@ __device__ __forceinline__ void cluster_exchange_wait(uint32_t bar) {
 #define MFR_CLUSTER_MIN_BLOCKS 2
 #endif
 
-// SPLIT (one chunk, top-k > 16): each partial's routes are split over S = p.route_groups thread groups of
+// SPLIT (one chunk, top-k > 8): each partial's routes are split over S = p.route_groups thread groups of
 // SV threads, group s loading routes 8s .. 8s+7 of its vector, so every row is in flight in one round;
 // groups s > 0 stage their raw rows in shared memory and group 0 runs the whole chain in route order.
 template <typename A, int KC, int MINB, bool REGS, bool SPLIT = false>

@@ -50,7 +50,7 @@ cudaError_t launch_cluster_kernel(int act_dtype, const KParams& p, const LaunchG
 // CTAs are small); 16 in flight.
 // The latency form is the one-chunk form with the route entries held in registers and branch-free
 // predicated row loads, for grids that put at most 256 gathering threads on an SM.
-// The split form (one chunk, top-k > 16) spreads each partial's routes over several thread groups.
+// The split form (one chunk, top-k > 8) spreads each partial's routes over several thread groups.
 enum ClusterForm {
   kClusterForm8 = 0,
   kClusterForm8OneChunk = 1,
