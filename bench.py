@@ -288,6 +288,11 @@ def run_case(spec: str, reps: int):
     import moe_finalize_residual_gb300 as mfr
     torch.cuda.set_device(0)
     base = dict(HEADLINE) if family == "decode" else {k: v for k, v in synth.CONFIGS[family].items() if k != "Ts"}
+    if family == "highk":  # the (H, E, K) shape with this H (default: the first)
+        shape = next((s for s in synth.HIGHK_SHAPES if s[0] == H), synth.HIGHK_SHAPES[0])
+        base.update(H=shape[0], E=shape[1], K=shape[2])
+    elif family == "masked":  # top-10, four partials, bf16 activations and scales
+        base.update(K=10, R=4, act_dtype=torch.bfloat16, scale_dtype=torch.bfloat16)
     if H:
         base["H"] = H
     c = synth.make_case(f"{family}-T{T}", T=T, device="cuda", **base)
@@ -574,8 +579,8 @@ def main():
                     help="write the extras (sweep, every config case, bandwidth grid, unfused pair) as JSON here")
     ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle time per cpu_baseline leg")
     ap.add_argument("--case", default=None, metavar="FAMILY:T[:H[:QUANT[:KERNEL]]]",
-                    help="run one workload --steps times without timing (for profilers), e.g. decode:128 or "
-                         "bandwidth:1024:7168:none:stream")
+                    help="run one workload --steps times without timing (for profilers), e.g. decode:128, "
+                         "bandwidth:1024:7168:none:bulk or highk:1:4096 (the high-top-k shape with that H)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.case:
