@@ -255,18 +255,10 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
       *xr = make_uint4(Act<A>::pack(a[0], a[1]), Act<A>::pack(a[2], a[3]), Act<A>::pack(a[4], a[5]),
                        Act<A>::pack(a[6], a[7]));
     }
-  } else
-  for (int ch = 0; ch < NCH; ++ch) {
-    const int vec = vec0 + ch * SV;
-    if (!in_group || vec >= nvec) break;
-    float2 acc[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
-    if constexpr (REGS)
-      for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain_regs<A, KC>(P, H, p.K, vec, rt, k0, acc);
-    else
-      for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain<A, KC>(P, H, p.K, vec, rt, k0, acc);
-    if (ch == 0) cp_async_wait_all();
+  }
+  // A chunk's partial row p_r from the FMA chain: times the routed scaling factor, plus the shared row,
+  // rounded once, into the chunk's exchange buffer.
+  auto finish_chunk = [&](int ch, float2 acc[4]) {
     uint4* xr = &xch[(ch * p.R + r) * SV + v];
     float shv[8];
     unpack8<A>(*xr, shv);
@@ -280,51 +272,73 @@ __global__ void __launch_bounds__(kClusterMaxThreads, MINB) cluster_finalize_ker
     }
     *xr = make_uint4(Act<A>::pack(a[0], a[1]), Act<A>::pack(a[2], a[3]), Act<A>::pack(a[4], a[5]),
                      Act<A>::pack(a[6], a[7]));
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  // The next kernel on the stream may launch now (programmatic dependent launch).  Triggering here,
-  // after the gather, rather than at kernel start measured faster at 16 tokens (4.66 against 5.51 µs,
-  // L2-warm) and the same elsewhere: launched at start, the next launches' CTAs pile up on the SMs
-  // while this one still gathers.
-  if (p.pdl) pdl_launch_dependents();
-
-  // The (chunk, vector) items of this CTA, spread over all its threads (item i to thread i mod the
-  // block; consecutive threads take consecutive vectors): rank sum in order 0..R-1, residual add (kept
-  // in place of the residual slice for the epilogue), sum of squares.
+  };
+  // The (chunk, vector) items [it0, it1) of this CTA, spread over all its threads (item i to thread i mod
+  // the block; consecutive threads take consecutive vectors): rank sum in order 0..R-1, residual add
+  // (kept in place of the residual slice for the epilogue), sum of squares.
   const int nitems = NCH * SV;
   const int vbase = static_cast<int>(crank) * NCH * SV;  // the CTA's first vector
   float ss = 0.0f;
-  for (int it = tid; it < nitems; it += nthreads) {
-    const int ch = it / SV, vv = it - ch * SV;
-    if (vbase + it >= nvec) break;  // (vector vbase + it; later items are further along)
-    float2 S[4];
+  auto items = [&](int it0, int it1) {
+    for (int it = it0 + tid; it < it1; it += nthreads) {
+      const int ch = it / SV, vv = it - ch * SV;
+      if (vbase + it >= nvec) break;  // (vector vbase + it; later items are further along)
+      float2 S[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) S[i] = make_float2(0.0f, 0.0f);
-    for (int rr = 0; rr < p.R; ++rr) {
-      float2 pr[4];
-      unpack_pairs<A>(xch[(ch * p.R + rr) * SV + vv], pr);
+      for (int i = 0; i < 4; ++i) S[i] = make_float2(0.0f, 0.0f);
+      for (int rr = 0; rr < p.R; ++rr) {
+        float2 pr[4];
+        unpack_pairs<A>(xch[(ch * p.R + rr) * SV + vv], pr);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) S[i] = __fadd2_rn(S[i], pr[i]);
+        for (int i = 0; i < 4; ++i) S[i] = __fadd2_rn(S[i], pr[i]);
+      }
+      if (p.finalize_out != nullptr)  // the finalized output S, rounded once
+        *reinterpret_cast<uint4*>(p.finalize_out + (static_cast<int64_t>(t) * H + (vbase + it) * 8) * 2) =
+            make_uint4(Act<A>::pack(S[0].x, S[0].y), Act<A>::pack(S[1].x, S[1].y), Act<A>::pack(S[2].x, S[2].y),
+                       Act<A>::pack(S[3].x, S[3].y));
+      if (p.fin_only) continue;
+      float2 res[4];
+      unpack_pairs<A>(res_s[it], res);
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = round_pair<A>(__fadd2_rn(round_pair<A>(S[i]), res[i]));
+        ss = __fmaf_rn(x.x, x.x, ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
+        ss = __fmaf_rn(x.y, x.y, ss);
+        w[i] = Act<A>::pack(x.x, x.y);
+      }
+      // kept for the epilogue, which writes it out with norm_out after the cluster exchange (the stores
+      // would otherwise sit between the items and the exchange on the critical path)
+      res_s[it] = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    if (p.finalize_out != nullptr)  // the finalized output S, rounded once
-      *reinterpret_cast<uint4*>(p.finalize_out + (static_cast<int64_t>(t) * H + (vbase + it) * 8) * 2) =
-          make_uint4(Act<A>::pack(S[0].x, S[0].y), Act<A>::pack(S[1].x, S[1].y), Act<A>::pack(S[2].x, S[2].y),
-                     Act<A>::pack(S[3].x, S[3].y));
-    if (p.fin_only) continue;
-    float2 res[4];
-    unpack_pairs<A>(res_s[it], res);
-    uint32_t w[4];
+  };
+  // The next kernel on the stream may launch once the gather is done (programmatic dependent launch).
+  // Triggering after the gather rather than at kernel start measured faster at 16 tokens (4.66 against
+  // 5.51 µs, L2-warm) and the same elsewhere: launched at start, the next launches' CTAs pile up on the
+  // SMs while this one still gathers.
+  if constexpr (SPLIT) {
+    cp_async_wait_all();
+    __syncthreads();
+    if (p.pdl) pdl_launch_dependents();
+    items(0, nitems);
+  } else {
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int vec = vec0 + ch * SV;
+      if (!in_group || vec >= nvec) break;
+      float2 acc[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 x = round_pair<A>(__fadd2_rn(round_pair<A>(S[i]), res[i]));
-      ss = __fmaf_rn(x.x, x.x, ss);  // x*x is exact for 16-bit x, so this equals ss + x*x
-      ss = __fmaf_rn(x.y, x.y, ss);
-      w[i] = Act<A>::pack(x.x, x.y);
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
+      if constexpr (REGS)
+        for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain_regs<A, KC>(P, H, p.K, vec, rt, k0, acc);
+      else
+        for (int k0 = 0; k0 < p.K; k0 += KC) gather_chain<A, KC>(P, H, p.K, vec, rt, k0, acc);
+      if (ch == 0) cp_async_wait_all();
+      finish_chunk(ch, acc);
     }
-    // kept for the epilogue, which writes it out with norm_out after the cluster exchange (the stores
-    // would otherwise sit between the items and the exchange on the critical path)
-    res_s[it] = make_uint4(w[0], w[1], w[2], w[3]);
+    cp_async_wait_all();
+    __syncthreads();
+    if (p.pdl) pdl_launch_dependents();
+    items(0, nitems);
   }
 
   if (p.fin_only) return;  // finalize-only: no residual, RMSNorm or quantisation (the same for all threads)
