@@ -17,7 +17,10 @@
 //    shared-row step, the rounding of a finished partial into the rank sum, and the residual row that
 //    closes the pass), and releases the stage.  After a token's last pass the warps meet on an
 //    mbarrier to add their sums of squares in warp order, and write norm_out and the quantised output
-//    from the kept residual_out while the producer is already streaming the next token's rows.
+//    from the kept residual_out while the copy warp is already streaming the next token's rows.
+//
+// The compute warps are 8 to 14, as the planner chooses for the row width (the row's 16-byte columns
+// filling the threads evenly), so a thread's column offsets come from the launch parameters.
 //
 // Prior art: flashinfer PR #3385 (TMA / mbarrier staging of the RMSNorm inputs); flashinfer PR #6546
 // (the large-batch finalizeKernelVecLoad path).  The arithmetic is that of flashinfer PR #6631,
