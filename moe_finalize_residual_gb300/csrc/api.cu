@@ -184,6 +184,9 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 #ifndef MFR_CLUSTER_BLOCK
 #define MFR_CLUSTER_BLOCK 512
 #endif
+#ifndef MFR_CLUSTER_ALT_BLOCK
+#define MFR_CLUSTER_ALT_BLOCK 384  // the smaller CTA size tried for multi-chunk plans (0: none)
+#endif
 #ifndef MFR_CLUSTER_CTAS_PER_SM
 #define MFR_CLUSTER_CTAS_PER_SM 2
 #endif
@@ -201,14 +204,14 @@ constexpr int kMaxCluster = MFR_CLUSTER_MAX_SIZE;
 // This plans one form of the kernel (kc routes in flight per thread) and reports how many waves of
 // resident clusters its grid takes.
 bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, int split, KParams* p, LaunchGeom* g,
-                       int64_t* waves_out) {
+                       int64_t* waves_out, int block_pref = MFR_CLUSTER_BLOCK) {
   const int nvec = a->H / 8;
   const int unit = (a->H % 16 == 0) ? 2 : 1;  // slices start on 16-element blocks when H allows
   const int R = a->R;
   const int RS = R * split;                   // thread groups: partials x route groups (split form)
   const int sv_max = (kClusterMaxThreads / RS) / unit * unit;
   if (sv_max < unit) return false;
-  const int sv_soft = std::min(sv_max, std::max(unit, (MFR_CLUSTER_BLOCK / RS) / unit * unit));
+  const int sv_soft = std::min(sv_max, std::max(unit, (block_pref / RS) / unit * unit));
   // About two CTAs per SM in all: c_goal CTAs per token, each covering nchunk chunks of sv vectors.
   // Few tokens: one chunk, the row spread over up to kMaxCluster CTAs.  More tokens: fewer CTAs per
   // token, each looping over several chunks.  More CTAs per token when shared memory is short.
@@ -309,9 +312,33 @@ bool plan_cluster_form(const mfr_args* a, const DeviceInfo& d, int dev, int kc, 
 // measured faster (top-10, R=4, H=7168: T=128 14.2 against 15.6 µs, T=16 6.1 against 6.3; top-16,
 // R=4, T=64: 10.6 against 12.9), while small blocks keep the single round (top-16, R=1, H=3584,
 // T=128: 5.4 against 7.3).  Larger top-k: sixteen in flight.
+// Row loads on the busiest SM for a one-wave plan: its CTAs x chunks x threads (each thread one 16-byte
+// vector of one route per chunk).
+int64_t busiest_sm_loads(const mfr_args* a, const DeviceInfo& d, const KParams& p, const LaunchGeom& g) {
+  const int64_t per_sm = (static_cast<int64_t>(g.grid) + d.sms - 1) / d.sms;
+  return per_sm * p.nchunk * static_cast<int64_t>(p.slice_vec) * a->R;
+}
+
 bool plan_cluster(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, LaunchGeom* g) {
   int64_t waves = 0;
-  if (a->K <= 8) return plan_cluster_form(a, d, dev, 8, 1, p, g, &waves);
+  if (a->K <= 8) {
+    if (!plan_cluster_form(a, d, dev, 8, 1, p, g, &waves)) return false;
+    // Several chunks per CTA: smaller CTAs may spread the same rows over more SMs.  Take the 384-thread
+    // plan when its busiest SM issues fewer row loads in one wave (decode T=64: C=4 x 384 threads
+    // against C=3 x 512, 6.59 against 7.70 us L2-warm, 9.11 against 9.44 L2-cold); on a tie keep the
+    // larger CTAs, which take fewer chunk rounds (T=128: 14.37 against 13.79 us L2-cold).
+    if (MFR_CLUSTER_ALT_BLOCK > 0 && p->nchunk > 1 && waves == 1) {
+      KParams p2 = *p;
+      LaunchGeom g2{};
+      int64_t w2 = 0;
+      if (plan_cluster_form(a, d, dev, 8, 1, &p2, &g2, &w2, MFR_CLUSTER_ALT_BLOCK) && w2 == 1 &&
+          busiest_sm_loads(a, d, p2, g2) < busiest_sm_loads(a, d, *p, *g)) {
+        *p = p2;
+        *g = g2;
+      }
+    }
+    return true;
+  }
   // Top-k > 8: the routes of a partial split over thread groups, when that plans one chunk in one wave.
   // L2-warm, same box: top-32 H=4096 T=1 5.77 -> 4.35 us; top-22 H=2048 T=1 5.11 -> 3.71; top-16 H=3584
   // T=1 4.10 -> 3.40, T=64 4.52 -> 4.12; top-10 R=2 T=1 3.63 -> 3.30 (never slower where it applies).
