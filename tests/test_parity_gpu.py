@@ -257,6 +257,19 @@ def test_cluster_plans_use_chunks():
         assert plan["grid"] == T * plan["cluster"] and plan["grid"] <= max(2 * sms, T), plan
 
 
+def test_cluster_cta_size_choice():
+    """Multi-chunk plans take 384-thread CTAs when the busiest SM then issues fewer row loads (decode T=64
+    on 152 SMs: 4 CTAs of 384 threads per token, two chunks each, against 3 of 512), and keep 512
+    threads on a tie (T=128: 2 CTAs of 512 threads, three chunks)."""
+    import moe_finalize_residual_gb300 as mfr
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected plans are those of a 152-SM GB300")
+    for T, want in ((64, (384, 4, 2)), (128, (512, 2, 3))):
+        case = synth.make_case("p", T=T, H=6144, K=8, R=4, E=64, shared=True, device="cuda")
+        plan = mfr.moe_finalize_plan(partials_of(case), case.residual, case.gamma)
+        assert (plan["block"], plan["cluster"], plan["stages"]) == want, plan
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_single_route_identity(kernel):
     case = synth.make_case("id", T=9, H=512, K=1, R=1, E=8, scale_dtype=None, rsf=1.0)
