@@ -463,7 +463,7 @@ bool plan_bulk(const mfr_args* a, const DeviceInfo& d, int dev, KParams* p, Laun
     const int bar_bytes = 8 * (2 * nst + 2 * 4 + 2) + 8;  // stages, lists, the token meeting; abort flag
     const int off_ring = align_up(off_bar + bar_bytes, 16);
     const int off_stash = align_up(off_ring + 4 * ring_bytes, 16);
-    const int off_sred = align_up(off_stash + a->H * 2, 16);
+    const int off_sred = align_up(off_stash + 2 * a->H * 2, 16);  // two stash buffers (by token parity)
     const int off_stage = align_up(off_sred + 2 * 32 * 4, 128);
     const int room = d.smem_optin - off_stage;
     const int sr = std::min(8, room / (nst * slot_bytes));

@@ -16,8 +16,9 @@
 //    waits on the stage's barrier, runs the partial's FP32 fused multiply-adds on its columns (or the
 //    shared-row step, the rounding of a finished partial into the rank sum, and the residual row that
 //    closes the pass), and releases the stage.  After a token's last pass the warps meet on an
-//    mbarrier to add their sums of squares in warp order, and write norm_out and the quantised output
-//    from the kept residual_out while the copy warp is already streaming the next token's rows.
+//    mbarrier to add their sums of squares in warp order.  The token's norm_out and quantised output
+//    are then written from the kept residual_out (two buffers, by token parity) in slices between the
+//    next token's stages, so the copy warp's ring keeps draining across the token boundary.
 //
 // The compute warps are 8 to 14, as the planner chooses for the row width (the row's 16-byte columns
 // filling the threads evenly), so a thread's column offsets come from the launch parameters.
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(32 * (2 + kBulkMaxComputeWarps), 1) bulk_final
     const int jt = tid - 64;                  // owns 16-byte columns jt + kNCT * q of a pass
     const int cw = warp - 2;
     const float qscale = (p.quant != MFR_QUANT_NONE) ? *p.quant_scale : 1.0f;
-    uint8_t* stash = smem + p.off_stash;      // the token's residual_out, for the epilogue
+    uint8_t* stash0 = smem + p.off_stash;     // [2][H]: a token's residual_out, by token parity, for its epilogue
     float* sred = reinterpret_cast<float*>(smem + p.off_sred);  // [2][32] warp sums by token parity
     auto colmask = [&](int ps) -> uint32_t {
       const int lim = min(W, H - ps * W);
@@ -226,6 +227,28 @@ __global__ void __launch_bounds__(32 * (2 + kBulkMaxComputeWarps), 1) bulk_final
       for (int q = 0; q < Q; ++q)
         if ((jt + q * kNCT) * 8 < lim) m |= 1u << q;
       return m;
+    };
+    // A token's epilogue (norm_out and the quantised output) runs while the next token's rows stream in:
+    // one slice (one column of one pass) after each stage the warp releases, the rest before that
+    // token's own sums of squares meet.  Each thread reads back only the stash columns it wrote, and the
+    // two stash buffers alternate by token, so the slices need no barrier.
+    int pend_t = -1;           // token whose epilogue is pending, or -1
+    int pend_i = 0;            // its place in this CTA's sequence (stash parity)
+    int pend_k = 0;            // its next slice: pass pend_k / Q, column pend_k % Q
+    float pend_rstd = 0.0f;
+    const int nslices = npass * Q;
+    auto epi_slice = [&]() {
+      const int ps = pend_k / Q, q = pend_k - ps * Q;
+      const int h = ps * W + (jt + q * kNCT) * 8;
+      const bool active = (colmask(ps) >> q) & 1u;
+      const uint8_t* st = stash0 + static_cast<int64_t>(pend_i & 1) * H * 2;
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, g[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (active) {
+        unpack8<A>(*reinterpret_cast<const uint4*>(st + static_cast<int64_t>(h) * 2), x);
+        unpack8<A>(ldg16(p.gamma + static_cast<int64_t>(h) * 2), g);
+      }
+      epilogue<A, 8>(p, pend_t, h, active, x, g, pend_rstd, qscale);  // all lanes (NVFP4 shuffles)
+      ++pend_k;
     };
     float2 acc[Q * 4], S[Q * 4];
 #pragma unroll
@@ -240,6 +263,7 @@ __global__ void __launch_bounds__(32 * (2 + kBulkMaxComputeWarps), 1) bulk_final
       const uint8_t* e = ring0 + slot * p.ring_bytes;
       const int n = *reinterpret_cast<const int*>(e);
       const RowEntry* list = reinterpret_cast<const RowEntry*>(e + 16);
+      uint8_t* stash = stash0 + static_cast<int64_t>(i & 1) * H * 2;
       float ss = 0.0f;
       for (int ps = 0; ps < npass && ok; ++ps) {
         const uint32_t cmask = colmask(ps);
@@ -326,11 +350,13 @@ __global__ void __launch_bounds__(32 * (2 + kBulkMaxComputeWarps), 1) bulk_final
             cs = 0;
             cpar ^= 1u;
           }
+          if (pend_t >= 0 && pend_k < nslices) epi_slice();  // the previous token's epilogue, a slice
         }
       }
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(lempty0 + 8u * slot);  // the list is no longer read
+      while (pend_t >= 0 && pend_k < nslices) epi_slice();
       if (p.fin_only) continue;
       // Token done: add the warps' sums of squares in warp order (the warps meet on an mbarrier,
       // double-buffered by token parity, so the wait is bounded), then norm_out and the quantised output.
@@ -340,25 +366,19 @@ __global__ void __launch_bounds__(32 * (2 + kBulkMaxComputeWarps), 1) bulk_final
         rb[cw] = wsum;
         mbar_arrive(meet0 + 8u * (i & 1));
       }
-      if (!warp_wait_phase(meet0 + 8u * (i & 1), static_cast<uint32_t>(i >> 1) & 1u, abort_flag)) break;
+      if (!warp_wait_phase(meet0 + 8u * (i & 1), static_cast<uint32_t>(i >> 1) & 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
       float tot = 0.0f;
       for (int w2 = 0; w2 < kNCW; ++w2) tot = __fadd_rn(tot, rb[w2]);
-      const float rstd = rms_rstd(tot, H, p.eps);
-      for (int ps = 0; ps < npass; ++ps) {
-        const uint32_t m = colmask(ps);
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-          const int h = ps * W + (jt + q * kNCT) * 8;
-          const bool active = (m >> q) & 1u;
-          float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, g[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (active) {
-            unpack8<A>(*reinterpret_cast<const uint4*>(stash + static_cast<int64_t>(h) * 2), x);
-            unpack8<A>(ldg16(p.gamma + static_cast<int64_t>(h) * 2), g);
-          }
-          epilogue<A, 8>(p, t, h, active, x, g, rstd, qscale);
-        }
-      }
+      pend_rstd = rms_rstd(tot, H, p.eps);
+      pend_t = t;
+      pend_i = i;
+      pend_k = 0;
     }
+    if (ok)  // the last token's epilogue
+      while (pend_t >= 0 && pend_k < nslices) epi_slice();
   }
   __syncthreads();
 }
