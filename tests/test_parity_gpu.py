@@ -101,6 +101,29 @@ def test_quant_small(T, act, kernel, quant, layout):
     check_quant(res, act, quant, qs, layout, T, case.H, want_norm=want["norm_out"])
 
 
+@pytest.mark.parametrize("quant,layout", [("none", "row_major")] + QUANTS)
+@pytest.mark.parametrize("H", [6144, 16400])
+def test_bulk_several_tokens_per_cta(H, quant, layout):
+    """The bulk kernel with two or three tokens per CTA, so each token's epilogue is written between the
+    next token's stages from alternating residual_out buffers; whole-row passes (H=6144) and two ragged
+    passes (H=16400); every output form; every token against the oracle."""
+    import moe_finalize_residual_gb300 as mfr
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = 2 * sms + 37
+    case = synth.make_case("bulkmt", T=T, H=H, K=4, R=2, E=32, rsf=2.5, shared=True, mask_quarter=True)
+    g = on_gpu(case)
+    plan = mfr.moe_finalize_plan(partials_of(g), g.residual, g.gamma, kernel="bulk")
+    assert plan["kernel"] == "bulk" and plan["grid"] < T, plan
+    assert (plan["chunk"] < H) == (H > 14336), plan
+    want = oracle.finalize(case)
+    qs = quant_scale_for(want["norm_out"], case.act_dtype, quant) if quant != "none" else None
+    res = run(g, kernel="bulk", quant=quant, qscale=qs, sf_layout=layout)
+    assert res.guards_ok
+    check_against_oracle(case, res, want)
+    if quant != "none":
+        check_quant(res, case.act_dtype, quant, qs, layout, T, H, want_norm=want["norm_out"])
+
+
 @pytest.mark.parametrize("quant,layout", QUANTS)
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_quant_without_norm_out(kernel, quant, layout):
