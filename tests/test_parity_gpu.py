@@ -615,6 +615,40 @@ def test_tp_one_shot_emulated_on_one_gpu(R, kernel):
         check_against_oracle(case, Result(bits16(ro), bits16(no), None, None, True), want)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("quant,layout", QUANTS)
+def test_tp_one_shot_quantised(quant, layout, kernel):
+    """The tensor-parallel path with a quantised output: every rank's fused call over the exchanged slots
+    gives the oracle's residual_out bit for bit, norm_out within 1 ulp, and the quantised bytes and block
+    scales of the oracle's quantiser applied to its own norm_out."""
+    import moe_finalize_residual_gb300 as mfr
+    from moe_finalize_residual_gb300 import tp
+    R = 2
+    case = synth.make_case("tpq", T=21, H=1024, K=6, R=R, E=32, rsf=2.5, shared=True, mask_quarter=True)
+    g = on_gpu(case)
+    parts = partials_of(g)
+    slots = [mfr.moe_finalize_routed([parts[r]], routed_scaling_factor=g.rsf, kernel=kernel) for r in range(R)]
+    want = oracle.finalize(case)
+    qs = quant_scale_for(want["norm_out"], case.act_dtype, quant)
+    for r in range(R):
+        ro, no, qo, sf = tp.tp_finalize_fused(parts[r], g.residual, g.gamma, routed_scaling_factor=g.rsf, eps=g.eps,
+                                              exchange=lambda p_r, group: slots, kernel=kernel, quant_mode=quant,
+                                              quant_scale=qs, sf_layout=layout)
+        torch.cuda.synchronize()
+        from helpers import Result
+        res = Result(bits16(ro), bits16(no), qo.cpu().numpy(), None if sf is None else sf.cpu().numpy(), True)
+        check_against_oracle(case, res, want)
+        if quant == "fp8":
+            check_quant(res, case.act_dtype, quant, qs, layout, case.T, case.H, want_norm=want["norm_out"])
+        else:  # the binding zero-fills the padding of a scale buffer it allocates
+            lay = oracle.SF_ROW_MAJOR if layout == "row_major" else oracle.SF_SWIZZLED_128x4
+            q_own, sf_own = oracle.quantize(res.norm_out, case.act_dtype, oracle.QUANT_NVFP4, qs, lay)
+            assert np.array_equal(res.quant_out.reshape(q_own.shape), q_own)
+            written = np.zeros(oracle.sf_bytes(case.T, case.H, lay), dtype=bool)
+            written[oracle.sf_offsets(case.T, case.H, lay).reshape(-1)] = True
+            assert np.array_equal(res.sf_out[written], sf_own[written]) and np.all(res.sf_out[~written] == 0)
+
+
 # ------------------------------------------------------------------------------------------------------
 # Finalize-only mode: the rounded rank sum S (p_0 for one partial), no residual / RMSNorm / quant.
 
